@@ -1,0 +1,232 @@
+"""ctypes shim over the CPU oracle (``ep_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers.  The product library never
+imports, links or runs anything in this folder.
+
+The shim only marshals numpy arrays; every step of the arithmetic is in the C
+file.  The shared object is built from source with gcc on first use (or by
+``build_oracle()``), with ``-ffp-contract=off`` so no multiply-add is fused
+unless the C code asks for it.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_DIR = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_DIR, "ep_oracle.c")
+_LIB = os.path.join(_DIR, "libep_oracle.so")
+
+OK, ERR_INVALID_ARG, ERR_EXPERT_RANGE, ERR_DUP_EXPERT, ERR_CAPACITY = range(5)
+
+
+def build_oracle(force: bool = False) -> str:
+    """Compile ``ep_oracle.c`` into ``libep_oracle.so`` next to it."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(
+        os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_DIR, "ep_oracle.h"))
+    ):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+             "-fPIC", "-shared", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(build_oracle())
+        _declare(_lib)
+    return _lib
+
+
+_p = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+
+
+def _declare(L):
+    L.oracle_bf16_to_f32.restype = ctypes.c_float
+    L.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    L.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    L.oracle_e4m3_to_f32.restype = ctypes.c_float
+    L.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    L.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+    L.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+    for name in ("oracle_f32_to_bf16_n", "oracle_bf16_to_f32_n",
+                 "oracle_f32_to_e4m3_n", "oracle_e4m3_to_f32_n"):
+        getattr(L, name).restype = None
+        getattr(L, name).argtypes = [_i64, _p, _p]
+    L.oracle_recv_capacity.restype = _i64
+    L.oracle_recv_capacity.argtypes = [_i32, _i32, _i32, _i32]
+    L.oracle_layout.restype = ctypes.c_int
+    L.oracle_layout.argtypes = [_i32, _i32, _i32, _i32, _i32, _p, _i64] + [_p] * 8
+    L.oracle_dispatch_bf16.restype = None
+    L.oracle_dispatch_bf16.argtypes = [_i32, _i32, _i32, _i32, _p, _p, _p, _p, _p,
+                                       ctypes.c_int, _p, _p]
+    L.oracle_dispatch_fp8.restype = None
+    L.oracle_dispatch_fp8.argtypes = [_i32, _i32, _i32, _i32, _p, _p, _p, _p, _p,
+                                      ctypes.c_int, _p, _p, _p]
+    L.oracle_combine.restype = None
+    L.oracle_combine.argtypes = [_i32, _i32, _i32, _p, _p, _p, _p]
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---- scalar codecs (vectorised by looping in Python: small inputs only) ----
+
+def bf16_to_f32(h) -> float:
+    return lib().oracle_bf16_to_f32(int(h))
+
+
+def f32_to_bf16(f) -> int:
+    return lib().oracle_f32_to_bf16(float(np.float32(f)))
+
+
+def e4m3_to_f32(c) -> float:
+    return lib().oracle_e4m3_to_f32(int(c))
+
+
+def f32_to_e4m3(v) -> int:
+    return lib().oracle_f32_to_e4m3(float(np.float32(v)))
+
+
+def _map(fn, a, in_dtype, out_dtype):
+    a = _c(a, in_dtype)
+    out = np.empty(a.shape, out_dtype)
+    getattr(lib(), fn)(a.size, _ptr(a), _ptr(out))
+    return out
+
+
+def f32_to_bf16_array(a) -> np.ndarray:
+    return _map("oracle_f32_to_bf16_n", a, np.float32, np.uint16)
+
+
+def bf16_to_f32_array(a) -> np.ndarray:
+    return _map("oracle_bf16_to_f32_n", a, np.uint16, np.float32)
+
+
+def f32_to_e4m3_array(a) -> np.ndarray:
+    return _map("oracle_f32_to_e4m3_n", a, np.float32, np.uint8)
+
+
+def e4m3_to_f32_array(a) -> np.ndarray:
+    return _map("oracle_e4m3_to_f32_n", a, np.uint8, np.float32)
+
+
+# ---- method -----------------------------------------------------------------
+
+def recv_capacity(max_tokens, num_topk, num_experts, alignment) -> int:
+    return int(lib().oracle_recv_capacity(max_tokens, num_topk, num_experts, alignment))
+
+
+def layout(topk_idx: np.ndarray, num_experts: int, num_ranks: int,
+           alignment: int, cap: Optional[int] = None) -> dict:
+    """Layout from the definition.  Returns a dict of numpy arrays + status."""
+    idx = _c(topk_idx, np.int64)
+    T, K = idx.shape
+    E, R, A = num_experts, num_ranks, alignment
+    if cap is None:
+        cap = recv_capacity(T, K, E, A)
+    out = dict(
+        expert_count=np.zeros(E, np.int32),
+        expert_start=np.zeros(E + 1, np.int32),
+        expert_end=np.zeros(E, np.int32),
+        rank_start=np.zeros(R + 1, np.int32),
+        tokens_per_rank=np.zeros(R, np.int32),
+        is_token_in_rank=np.zeros((T, R), np.uint8),
+        slot_of=np.zeros((T, K), np.int32),
+        src_info=np.zeros((cap, 2), np.int32),
+    )
+    st = lib().oracle_layout(
+        T, K, E, R, A, _ptr(idx), cap,
+        _ptr(out["expert_count"]), _ptr(out["expert_start"]), _ptr(out["expert_end"]),
+        _ptr(out["rank_start"]), _ptr(out["tokens_per_rank"]),
+        _ptr(out["is_token_in_rank"]), _ptr(out["slot_of"]), _ptr(out["src_info"]))
+    out["status"] = int(st)
+    out["cap"] = cap
+    return out
+
+
+def dispatch_bf16(x, topk_weights, lay: dict, zero_padding=False, fill=0xFFFF):
+    """Expanded bf16 dispatch; rows the method does not write keep ``fill``."""
+    x = _c(x, np.uint16)
+    T, H = x.shape
+    slot_of = _c(lay["slot_of"], np.int32)
+    K = slot_of.shape[1]
+    E = lay["expert_count"].shape[0]
+    cap = lay["cap"]
+    w = None if topk_weights is None else _c(topk_weights, np.float32)
+    recv_x = np.full((cap, H), fill, np.uint16)
+    recv_w = np.full(cap, np.nan, np.float32)
+    lib().oracle_dispatch_bf16(T, H, K, E, _ptr(x), _ptr(w), _ptr(slot_of),
+                               _ptr(_c(lay["expert_start"], np.int32)),
+                               _ptr(_c(lay["expert_end"], np.int32)),
+                               int(bool(zero_padding)), _ptr(recv_x), _ptr(recv_w))
+    return recv_x, recv_w
+
+
+def dispatch_fp8(x, topk_weights, lay: dict, zero_padding=False, fill=0xFF):
+    """Expanded dispatch with fused 1x128 E4M3 quantisation."""
+    x = _c(x, np.uint16)
+    T, H = x.shape
+    slot_of = _c(lay["slot_of"], np.int32)
+    K = slot_of.shape[1]
+    E = lay["expert_count"].shape[0]
+    cap = lay["cap"]
+    w = None if topk_weights is None else _c(topk_weights, np.float32)
+    recv_q = np.full((cap, H), fill, np.uint8)
+    recv_scale = np.full((cap, H // 128), np.nan, np.float32)
+    recv_w = np.full(cap, np.nan, np.float32)
+    lib().oracle_dispatch_fp8(T, H, K, E, _ptr(x), _ptr(w), _ptr(slot_of),
+                              _ptr(_c(lay["expert_start"], np.int32)),
+                              _ptr(_c(lay["expert_end"], np.int32)),
+                              int(bool(zero_padding)), _ptr(recv_q),
+                              _ptr(recv_scale), _ptr(recv_w))
+    return recv_q, recv_scale, recv_w
+
+
+def combine(expert_out, topk_weights, slot_of) -> np.ndarray:
+    """Combine from the definition: returns y (uint16 bf16 bits [T, H])."""
+    Y = _c(expert_out, np.uint16)
+    H = Y.shape[1]
+    slot_of = _c(slot_of, np.int32)
+    T, K = slot_of.shape
+    w = None if topk_weights is None else _c(topk_weights, np.float32)
+    y = np.zeros((T, H), np.uint16)
+    lib().oracle_combine(T, H, K, _ptr(Y), _ptr(w), _ptr(slot_of), _ptr(y))
+    return y
+
+
+def combine_tokens(expert_out, topk_weights, slot_of, tokens) -> np.ndarray:
+    """Combine for a sample of tokens only: the oracle's own definition applied
+    to the rows those tokens select, so that it can be checked at full size."""
+    tokens = np.asarray(tokens, dtype=np.int64)
+    so = np.asarray(slot_of)[tokens]
+    used = so >= 0
+    rows = so[used]
+    sub = np.full(so.shape, -1, np.int32)
+    sub[used] = np.arange(rows.size, dtype=np.int32)
+    Ysub = np.asarray(expert_out)[rows] if rows.size else np.zeros((0, np.asarray(expert_out).shape[1]), np.uint16)
+    w = None if topk_weights is None else np.asarray(topk_weights)[tokens]
+    if rows.size == 0:
+        Ysub = np.zeros((1, np.asarray(expert_out).shape[1]), np.uint16)
+    return combine(Ysub, w, sub)

@@ -1,0 +1,103 @@
+/*
+ * CPU oracle for the MoE dispatch / combine layout path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is a plain, slow, single-threaded
+ * restatement of what the method computes, used to check the CUDA library.
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+ * load it.  It shares no code, header, table or constant with the CUDA path.
+ *
+ * Sources (page title, section):
+ *  - "GPU Microarchitecture: DeepEP from First Principles", 1.1 (dispatch:
+ *    token-major -> destination-major -> expert-major), 1.2 (combine:
+ *    Output(T0) = 0.73 x Expert2(T0) + 0.27 x Expert7(T0)), 6.1 (layout
+ *    metadata: count, prefix sum, offset), 6.2 (identity metadata),
+ *    7.1 (count -> prefix sum -> scatter).
+ *  - "Deep Dive - DeepEP": "Dispatch: layout, move, and epilogue" (input
+ *    contract, -1 = unused, expanded mode, expert alignment, psum semantics),
+ *    "Combine: reverse routing plus reduction" (fp32 accumulation, one final
+ *    bf16 cast, the bf16 rounding formula), "Precision: FP8 on the wire, BF16
+ *    for the reduction" (one fp32 scale per 128 values), "A four-token routing
+ *    ledger" / "A runnable routing ledger" (owner rank = expert / experts per
+ *    rank, per-rank dedup, masked selections, padding), "EPHandle: route
+ *    metadata with a lifetime" (deterministic order by source-global order).
+ *
+ * Every function is pinned by the CPU test-suite against worked examples,
+ * closed forms, exhaustive codec checks and brute force; none is
+ * "parity unpinned".
+ */
+#ifndef EP_ORACLE_H
+#define EP_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  ORACLE_OK = 0,
+  ORACLE_ERR_INVALID_ARG = 1,
+  ORACLE_ERR_EXPERT_RANGE = 2,
+  ORACLE_ERR_DUP_EXPERT = 3,
+  ORACLE_ERR_CAPACITY = 4
+};
+
+/* ---- number formats ---------------------------------------------------- */
+float oracle_bf16_to_f32(uint16_t h);
+uint16_t oracle_f32_to_bf16(float f);   /* round to nearest even */
+float oracle_e4m3_to_f32(uint8_t c);
+uint8_t oracle_f32_to_e4m3(float v);    /* round to nearest even, satfinite */
+/* element-wise array forms of the four codecs above */
+void oracle_f32_to_bf16_n(int64_t n, const float *in, uint16_t *out);
+void oracle_bf16_to_f32_n(int64_t n, const uint16_t *in, float *out);
+void oracle_f32_to_e4m3_n(int64_t n, const float *in, uint8_t *out);
+void oracle_e4m3_to_f32_n(int64_t n, const uint8_t *in, float *out);
+
+/* ---- layout ------------------------------------------------------------ */
+/* Worst-case rows of the expert-major buffer: every (token, k) unmasked and
+ * every expert segment padded by alignment - 1 rows. */
+int64_t oracle_recv_capacity(int32_t max_tokens, int32_t num_topk,
+                             int32_t num_experts, int32_t alignment);
+
+/* topk_idx [T*K] int64 row-major.  Outputs (all caller-allocated):
+ * expert_count[E], expert_start[E+1], expert_end[E], rank_start[R+1],
+ * tokens_per_rank[R], is_token_in_rank[T*R], slot_of[T*K],
+ * src_info[2*cap] as (token, k) pairs; rows that carry no token are (-1,-1).
+ * Returns an ORACLE_* status; on error the outputs are unspecified. */
+int oracle_layout(int32_t T, int32_t K, int32_t E, int32_t R, int32_t A,
+                  const int64_t *topk_idx, int64_t cap,
+                  int32_t *expert_count, int32_t *expert_start,
+                  int32_t *expert_end, int32_t *rank_start,
+                  int32_t *tokens_per_rank, uint8_t *is_token_in_rank,
+                  int32_t *slot_of, int32_t *src_info);
+
+/* ---- dispatch ---------------------------------------------------------- */
+/* recv_x[slot_of[t,k]] = x[t] (raw bf16 bits); recv_w[slot] = w[t,k].
+ * With zero_padding, rows [expert_end[e], expert_start[e+1]) are zeroed and
+ * their recv_w set to 0.  w and recv_w may be NULL (then recv_w untouched). */
+void oracle_dispatch_bf16(int32_t T, int32_t H, int32_t K, int32_t E,
+                          const uint16_t *x, const float *w,
+                          const int32_t *slot_of, const int32_t *expert_start,
+                          const int32_t *expert_end, int zero_padding,
+                          uint16_t *recv_x, float *recv_w);
+
+/* Fused 1x128 FP8 E4M3 quantisation of each dispatched row:
+ * recv_q[slot, H] bytes, recv_scale[slot, H/128] fp32 (dequant multiplier). */
+void oracle_dispatch_fp8(int32_t T, int32_t H, int32_t K, int32_t E,
+                         const uint16_t *x, const float *w,
+                         const int32_t *slot_of, const int32_t *expert_start,
+                         const int32_t *expert_end, int zero_padding,
+                         uint8_t *recv_q, float *recv_scale, float *recv_w);
+
+/* ---- combine ----------------------------------------------------------- */
+/* y[t,i] = bf16( fold over k ascending, slot_of[t,k] >= 0, of
+ *               acc = fmaf(w[t,k], Y[slot_of[t,k], i], acc) ), acc0 = +0.
+ * w == NULL means every weight is 1 (plain sum of caller-weighted rows). */
+void oracle_combine(int32_t T, int32_t H, int32_t K, const uint16_t *Y,
+                    const float *w, const int32_t *slot_of, uint16_t *y);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EP_ORACLE_H */
