@@ -1,0 +1,289 @@
+"""Python binding of libep_gb300.so (MoE dispatch / combine layout on GB300).
+
+Two layers, both argument marshalling only -- every step of layout, dispatch
+and combine runs in the library's CUDA kernels:
+
+* ``ep_*`` functions with the C ABI's names and arguments (include/ep.h),
+  taking ``EpConfig`` / ``EpLayout`` ctypes structures and raw pointers.
+* A torch layer (``Config``, ``Layout``, ``get_layout``, ``dispatch``,
+  ``combine``) that allocates device buffers with torch, passes
+  ``tensor.data_ptr()`` and the current CUDA stream, and raises ``EpError``
+  on a non-zero status.  torch provides memory and streams, nothing else.
+
+There is no fallback: if the shared library is missing, importing this
+package raises.  Build it with ``python combine_get_layout_gb300/build_lib.py``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libep_gb300.so")
+
+EP_OK = 0
+EP_ERR_INVALID_ARG = 1
+EP_ERR_EXPERT_RANGE = 2
+EP_ERR_DUP_EXPERT = 3
+EP_ERR_CAPACITY = 4
+EP_ERR_CUDA = 5
+EP_ERR_TIMEOUT = 6
+
+# The entry points include/ep.h declares (kept in sync by a test).
+ABI_SYMBOLS = (
+    "ep_recv_capacity",
+    "ep_layout_workspace_bytes",
+    "ep_get_layout",
+    "ep_dispatch",
+    "ep_combine",
+    "ep_check_error",
+    "ep_selftest_wait_timeout",
+    "ep_status_str",
+)
+
+
+class EpConfig(ctypes.Structure):
+    _fields_ = [
+        ("max_tokens", ctypes.c_int32),
+        ("hidden", ctypes.c_int32),
+        ("num_topk", ctypes.c_int32),
+        ("num_experts", ctypes.c_int32),
+        ("num_ranks", ctypes.c_int32),
+        ("expert_alignment", ctypes.c_int32),
+        ("use_fp8_dispatch", ctypes.c_int32),
+        ("zero_padding", ctypes.c_int32),
+    ]
+
+
+class EpLayout(ctypes.Structure):
+    _fields_ = [
+        ("expert_count", ctypes.c_void_p),
+        ("expert_start", ctypes.c_void_p),
+        ("expert_end", ctypes.c_void_p),
+        ("rank_start", ctypes.c_void_p),
+        ("tokens_per_rank", ctypes.c_void_p),
+        ("is_token_in_rank", ctypes.c_void_p),
+        ("slot_of", ctypes.c_void_p),
+        ("src_info", ctypes.c_void_p),
+        ("err", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p),
+        ("num_tokens", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python combine_get_layout_gb300/build_lib.py` (nvcc, sm_103a)")
+    L = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    L.ep_recv_capacity.restype = i64
+    L.ep_recv_capacity.argtypes = [P(EpConfig)]
+    L.ep_layout_workspace_bytes.restype = i64
+    L.ep_layout_workspace_bytes.argtypes = [P(EpConfig)]
+    L.ep_get_layout.restype = i32
+    L.ep_get_layout.argtypes = [P(EpConfig), i32, vp, P(EpLayout), vp, vp]
+    L.ep_dispatch.restype = i32
+    L.ep_dispatch.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp, vp]
+    L.ep_combine.restype = i32
+    L.ep_combine.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp]
+    L.ep_check_error.restype = i32
+    L.ep_check_error.argtypes = [P(EpLayout), vp]
+    L.ep_selftest_wait_timeout.restype = i32
+    L.ep_selftest_wait_timeout.argtypes = [i64, vp, vp]
+    L.ep_status_str.restype = ctypes.c_char_p
+    L.ep_status_str.argtypes = [i32]
+    return L
+
+
+_lib = _load()
+
+
+def lib():
+    """The loaded ctypes library (for tests that call the ABI directly)."""
+    return _lib
+
+
+# ---- C-ABI names ------------------------------------------------------------
+
+def ep_recv_capacity(cfg: EpConfig) -> int:
+    return int(_lib.ep_recv_capacity(ctypes.byref(cfg)))
+
+
+def ep_layout_workspace_bytes(cfg: EpConfig) -> int:
+    return int(_lib.ep_layout_workspace_bytes(ctypes.byref(cfg)))
+
+
+def ep_get_layout(cfg, num_tokens, d_topk_idx, layout, h_expert_count, stream) -> int:
+    return int(_lib.ep_get_layout(ctypes.byref(cfg), num_tokens, d_topk_idx,
+                                  ctypes.byref(layout), h_expert_count, stream))
+
+
+def ep_dispatch(cfg, layout, d_x, d_topk_weights, d_recv_x, d_recv_scale,
+                d_recv_w, stream) -> int:
+    return int(_lib.ep_dispatch(ctypes.byref(cfg), ctypes.byref(layout), d_x,
+                                d_topk_weights, d_recv_x, d_recv_scale,
+                                d_recv_w, stream))
+
+
+def ep_combine(cfg, layout, d_expert_out, d_topk_weights, d_y, stream) -> int:
+    return int(_lib.ep_combine(ctypes.byref(cfg), ctypes.byref(layout),
+                               d_expert_out, d_topk_weights, d_y, stream))
+
+
+def ep_check_error(layout, stream) -> int:
+    return int(_lib.ep_check_error(ctypes.byref(layout), stream))
+
+
+def ep_selftest_wait_timeout(timeout_ns, d_err, stream) -> int:
+    return int(_lib.ep_selftest_wait_timeout(int(timeout_ns), d_err, stream))
+
+
+def ep_status_str(status: int) -> str:
+    return _lib.ep_status_str(int(status)).decode()
+
+
+# ---- torch layer ------------------------------------------------------------
+
+class EpError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        super().__init__(f"{what}: {ep_status_str(status)} ({status})")
+
+
+def _check(status: int, what: str):
+    if status != EP_OK:
+        raise EpError(status, what)
+
+
+@dataclasses.dataclass(frozen=True)
+class Config:
+    """Mirror of ep_config (see include/ep.h)."""
+
+    max_tokens: int
+    hidden: int
+    num_topk: int
+    num_experts: int
+    num_ranks: int
+    expert_alignment: int = 128
+    use_fp8_dispatch: bool = False
+    zero_padding: bool = False
+
+    def c(self) -> EpConfig:
+        return EpConfig(self.max_tokens, self.hidden, self.num_topk,
+                        self.num_experts, self.num_ranks, self.expert_alignment,
+                        int(self.use_fp8_dispatch), int(self.zero_padding))
+
+    @property
+    def capacity(self) -> int:
+        cap = ep_recv_capacity(self.c())
+        if cap < 0:
+            raise EpError(EP_ERR_INVALID_ARG, "config")
+        return cap
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Layout:
+    """Device buffers of one layout handle, allocated with torch."""
+
+    def __init__(self, cfg: Config, device="cuda"):
+        import torch
+
+        self.cfg = cfg
+        E, R, K, T = cfg.num_experts, cfg.num_ranks, cfg.num_topk, cfg.max_tokens
+        cap = cfg.capacity
+        ws = ep_layout_workspace_bytes(cfg.c())
+        i32 = dict(dtype=torch.int32, device=device)
+        self.expert_count = torch.zeros(E, **i32)
+        self.expert_start = torch.zeros(E + 1, **i32)
+        self.expert_end = torch.zeros(E, **i32)
+        self.rank_start = torch.zeros(R + 1, **i32)
+        self.tokens_per_rank = torch.zeros(R, **i32)
+        self.is_token_in_rank = torch.zeros((max(T, 1), R), dtype=torch.uint8, device=device)
+        self.slot_of = torch.full((max(T, 1), K), -1, **i32)
+        self.src_info = torch.full((cap, 2), -1, **i32)
+        self.err = torch.zeros(4, **i32)
+        self.workspace = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)
+        self.c = EpLayout(
+            _ptr(self.expert_count), _ptr(self.expert_start), _ptr(self.expert_end),
+            _ptr(self.rank_start), _ptr(self.tokens_per_rank),
+            _ptr(self.is_token_in_rank), _ptr(self.slot_of), _ptr(self.src_info),
+            _ptr(self.err), _ptr(self.workspace), 0, 0)
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.c.num_tokens)
+
+
+def get_layout(cfg: Config, topk_idx, layout: Optional[Layout] = None,
+               sync: bool = False, stream=None) -> Layout:
+    """ep_get_layout on an int64 CUDA tensor [T, K]."""
+    import numpy as np
+
+    if layout is None:
+        layout = Layout(cfg, device=topk_idx.device)
+    T = int(topk_idx.shape[0])
+    h = None
+    if sync:
+        h = np.zeros(cfg.num_experts, np.int32)
+    st = ep_get_layout(cfg.c(), T, _ptr(topk_idx.contiguous()) if T else None,
+                       layout.c, None if h is None else h.ctypes.data_as(ctypes.c_void_p),
+                       _stream(stream))
+    _check(st, "ep_get_layout")
+    layout.h_expert_count = h
+    return layout
+
+
+def dispatch(cfg: Config, layout: Layout, x, topk_weights=None, recv_x=None,
+             recv_scale=None, recv_w=None, want_weights: bool = True, stream=None):
+    """ep_dispatch.  x: bf16 CUDA tensor [T, H].  Returns (recv_x, recv_scale,
+    recv_w); recv_x is bf16 [cap, H] or uint8 (E4M3 bits) [cap, H]."""
+    import torch
+
+    cap, H = cfg.capacity, cfg.hidden
+    dev = x.device
+    if recv_x is None:
+        dt = torch.uint8 if cfg.use_fp8_dispatch else torch.bfloat16
+        recv_x = torch.empty((cap, H), dtype=dt, device=dev)
+    if cfg.use_fp8_dispatch and recv_scale is None:
+        recv_scale = torch.empty((cap, H // 128), dtype=torch.float32, device=dev)
+    if want_weights and topk_weights is not None and recv_w is None:
+        recv_w = torch.empty(cap, dtype=torch.float32, device=dev)
+    st = ep_dispatch(cfg.c(), layout.c, _ptr(x), _ptr(topk_weights), _ptr(recv_x),
+                     _ptr(recv_scale), _ptr(recv_w), _stream(stream))
+    _check(st, "ep_dispatch")
+    return recv_x, recv_scale, recv_w
+
+
+def combine(cfg: Config, layout: Layout, expert_out, topk_weights=None, y=None,
+            stream=None):
+    """ep_combine.  expert_out: bf16 CUDA tensor [cap, H]; returns bf16 [T, H]."""
+    import torch
+
+    T = layout.num_tokens
+    if y is None:
+        y = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device=expert_out.device)
+    st = ep_combine(cfg.c(), layout.c, _ptr(expert_out), _ptr(topk_weights),
+                    _ptr(y), _stream(stream))
+    _check(st, "ep_combine")
+    return y
+
+
+def check_error(layout: Layout, stream=None) -> int:
+    return ep_check_error(layout.c, _stream(stream))

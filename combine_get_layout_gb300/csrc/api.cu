@@ -1,0 +1,238 @@
+// extern "C" entry points of libep_gb300.so (declared in include/ep.h):
+// host-side validation, sizing, and launches on the caller's stream.  The
+// library holds no state besides a per-device property cache.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/ep.h"
+#include "ep_device.cuh"
+#include "ep_internal.h"
+
+namespace ep {
+
+constexpr int kMaxDevices = 64;
+
+const DeviceInfo& device_info() {
+  static DeviceInfo infos[kMaxDevices];
+  static std::once_flag once[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  std::call_once(once[dev], [dev] {
+    DeviceInfo& d = infos[dev];
+    d.sm_count = 1;
+    d.max_smem_optin = 48 * 1024;
+    d.smem_per_sm = 48 * 1024;
+    cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  });
+  return infos[dev];
+}
+
+static bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+static bool config_ok(const ep_config* c) {
+  if (c == nullptr) return false;
+  if (c->max_tokens < 0 || c->hidden < 8 || c->hidden % 8 != 0) return false;
+  if (c->hidden > (1 << 20)) return false;
+  if (c->num_topk < 1 || c->num_topk > 32) return false;
+  if (c->num_experts < 1 || c->num_experts > 2048) return false;
+  if (c->num_topk > c->num_experts) return false;
+  if (c->num_ranks < 1 || c->num_ranks > c->num_experts) return false;
+  if (c->num_experts % c->num_ranks != 0) return false;
+  if (c->expert_alignment < 1 || c->expert_alignment > 1024) return false;
+  if (c->use_fp8_dispatch != 0 && c->use_fp8_dispatch != 1) return false;
+  if (c->zero_padding != 0 && c->zero_padding != 1) return false;
+  if (c->use_fp8_dispatch && c->hidden % 128 != 0) return false;
+  // bf16 rows are staged whole in shared memory (two stages at least)
+  if (!c->use_fp8_dispatch && c->hidden > 49152) return false;
+  // all row indices fit in int32
+  const int64_t cap = int64_t(c->max_tokens) * c->num_topk +
+                      int64_t(c->num_experts) * (c->expert_alignment - 1);
+  if (cap >= (int64_t(1) << 31)) return false;
+  return true;
+}
+
+static int64_t capacity(const ep_config* c) {
+  return int64_t(c->max_tokens) * c->num_topk +
+         int64_t(c->num_experts) * (c->expert_alignment - 1);
+}
+
+static int32_t cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+static int32_t status_from_bits(int32_t bits) {
+  if (bits & ERRBIT_EXPERT_RANGE) return EP_ERR_EXPERT_RANGE;
+  if (bits & ERRBIT_DUP_EXPERT) return EP_ERR_DUP_EXPERT;
+  if (bits & ERRBIT_TIMEOUT) return EP_ERR_TIMEOUT;
+  return EP_OK;
+}
+
+static bool layout_ptrs_ok(const ep_layout* L) {
+  if (L == nullptr) return false;
+  const void* ps[] = {L->expert_count, L->expert_start, L->expert_end,
+                      L->rank_start, L->tokens_per_rank, L->is_token_in_rank,
+                      L->slot_of, L->src_info, L->err, L->workspace};
+  for (const void* p : ps)
+    if (p == nullptr || !aligned16(p)) return false;
+  return true;
+}
+
+}  // namespace ep
+
+using namespace ep;
+
+extern "C" {
+
+int64_t ep_recv_capacity(const ep_config* cfg) {
+  return config_ok(cfg) ? capacity(cfg) : -1;
+}
+
+int64_t ep_layout_workspace_bytes(const ep_config* cfg) {
+  if (!config_ok(cfg)) return -1;
+  const int tiles = layout_max_tiles(cfg->max_tokens, cfg->num_topk);
+  return layout_workspace_bytes(tiles, cfg->num_experts, cfg->num_ranks);
+}
+
+int32_t ep_get_layout(const ep_config* cfg, int32_t num_tokens,
+                      const int64_t* d_topk_idx, ep_layout* layout,
+                      int32_t* h_expert_count, void* stream) {
+  if (!config_ok(cfg) || !layout_ptrs_ok(layout)) return EP_ERR_INVALID_ARG;
+  if (num_tokens < 0 || num_tokens > cfg->max_tokens) return EP_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (d_topk_idx == nullptr || !aligned16(d_topk_idx)))
+    return EP_ERR_INVALID_ARG;
+  const int K = cfg->num_topk, E = cfg->num_experts, R = cfg->num_ranks;
+  const int max_tiles = layout_max_tiles(cfg->max_tokens, K);
+  LayoutArgs a;
+  a.topk_idx = d_topk_idx;
+  a.T = num_tokens;
+  a.K = K;
+  a.E = E;
+  a.R = R;
+  a.A = cfg->expert_alignment;
+  a.geom = layout_tiles(num_tokens > 0 ? num_tokens : 1, K);
+  if (a.geom.num_tiles > max_tiles) return EP_ERR_INVALID_ARG;
+  a.ws = carve_layout_workspace(layout->workspace, max_tiles, E, R);
+  a.expert_count = layout->expert_count;
+  a.expert_start = layout->expert_start;
+  a.expert_end = layout->expert_end;
+  a.rank_start = layout->rank_start;
+  a.tokens_per_rank = layout->tokens_per_rank;
+  a.slot_of = layout->slot_of;
+  a.src_info = layout->src_info;
+  a.err = layout->err;
+  a.is_token_in_rank = layout->is_token_in_rank;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_layout(a, s);
+  if (e != cudaSuccess) return EP_ERR_CUDA;
+  layout->num_tokens = num_tokens;
+  if (h_expert_count != nullptr) {
+    int32_t bits = 0;
+    e = cudaMemcpyAsync(h_expert_count, layout->expert_count, sizeof(int32_t) * E,
+                        cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(&bits, layout->err, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return EP_ERR_CUDA;
+    return status_from_bits(bits);
+  }
+  return EP_OK;
+}
+
+int32_t ep_dispatch(const ep_config* cfg, const ep_layout* layout,
+                    const void* d_x, const float* d_topk_weights,
+                    void* d_recv_x, float* d_recv_scale, float* d_recv_w,
+                    void* stream) {
+  if (!config_ok(cfg) || !layout_ptrs_ok(layout)) return EP_ERR_INVALID_ARG;
+  const int T = layout->num_tokens;
+  if (T < 0 || T > cfg->max_tokens) return EP_ERR_INVALID_ARG;
+  if (d_recv_x == nullptr || !aligned16(d_recv_x)) return EP_ERR_INVALID_ARG;
+  if (T > 0 && (d_x == nullptr || !aligned16(d_x))) return EP_ERR_INVALID_ARG;
+  if (d_topk_weights != nullptr && !aligned16(d_topk_weights)) return EP_ERR_INVALID_ARG;
+  if (d_recv_w != nullptr && !aligned16(d_recv_w)) return EP_ERR_INVALID_ARG;
+  if (d_recv_w != nullptr && d_topk_weights == nullptr) return EP_ERR_INVALID_ARG;
+  if (cfg->use_fp8_dispatch && (d_recv_scale == nullptr || !aligned16(d_recv_scale)))
+    return EP_ERR_INVALID_ARG;
+  DispatchArgs a;
+  a.x = d_x;
+  a.topk_weights = d_topk_weights;
+  a.slot_of = layout->slot_of;
+  a.expert_start = layout->expert_start;
+  a.expert_end = layout->expert_end;
+  a.T = T;
+  a.H = cfg->hidden;
+  a.K = cfg->num_topk;
+  a.E = cfg->num_experts;
+  a.fp8 = cfg->use_fp8_dispatch != 0;
+  a.zero_padding = cfg->zero_padding != 0;
+  a.recv_x = d_recv_x;
+  a.recv_scale = d_recv_scale;
+  a.recv_w = d_recv_w;
+  a.err = layout->err;
+  return cuda_status(launch_dispatch(a, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t ep_combine(const ep_config* cfg, const ep_layout* layout,
+                   const void* d_expert_out, const float* d_topk_weights,
+                   void* d_y, void* stream) {
+  if (!config_ok(cfg) || !layout_ptrs_ok(layout)) return EP_ERR_INVALID_ARG;
+  const int T = layout->num_tokens;
+  if (T < 0 || T > cfg->max_tokens) return EP_ERR_INVALID_ARG;
+  if (T > 0) {
+    if (d_expert_out == nullptr || !aligned16(d_expert_out)) return EP_ERR_INVALID_ARG;
+    if (d_y == nullptr || !aligned16(d_y)) return EP_ERR_INVALID_ARG;
+  }
+  if (d_topk_weights != nullptr && !aligned16(d_topk_weights)) return EP_ERR_INVALID_ARG;
+  CombineArgs a;
+  a.expert_out = d_expert_out;
+  a.topk_weights = d_topk_weights;
+  a.slot_of = layout->slot_of;
+  a.T = T;
+  a.H = cfg->hidden;
+  a.K = cfg->num_topk;
+  a.y = d_y;
+  return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t ep_check_error(const ep_layout* layout, void* stream) {
+  if (layout == nullptr || layout->err == nullptr) return EP_ERR_INVALID_ARG;
+  int32_t bits = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&bits, layout->err, sizeof(int32_t),
+                                  cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return EP_ERR_CUDA;
+  return status_from_bits(bits);
+}
+
+int32_t ep_selftest_wait_timeout(int64_t timeout_ns, int32_t* d_err, void* stream) {
+  if (d_err == nullptr || !aligned16(d_err)) return EP_ERR_INVALID_ARG;
+  if (timeout_ns < 1000 || timeout_ns > 1000000000) return EP_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_wait_selftest(uint64_t(timeout_ns), d_err, s);
+  int32_t bits = 0;
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&bits, d_err, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return EP_ERR_CUDA;
+  return status_from_bits(bits);
+}
+
+const char* ep_status_str(int32_t status) {
+  switch (status) {
+    case EP_OK: return "EP_OK";
+    case EP_ERR_INVALID_ARG: return "EP_ERR_INVALID_ARG";
+    case EP_ERR_EXPERT_RANGE: return "EP_ERR_EXPERT_RANGE";
+    case EP_ERR_DUP_EXPERT: return "EP_ERR_DUP_EXPERT";
+    case EP_ERR_CAPACITY: return "EP_ERR_CAPACITY";
+    case EP_ERR_CUDA: return "EP_ERR_CUDA";
+    case EP_ERR_TIMEOUT: return "EP_ERR_TIMEOUT";
+    default: return "EP_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

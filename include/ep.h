@@ -1,0 +1,207 @@
+/*
+ * ep.h -- C ABI of the GB300 MoE dispatch / combine layout library
+ * (libep_gb300.so, CUDA sm_103a).
+ *
+ * The library implements the data-parallel hot path of expert-parallel MoE
+ * communication as a layout transformation on ONE GPU: expert-parallel ranks
+ * are logical destination partitions of a single HBM buffer.
+ *
+ *   ep_get_layout : topk_idx            -> counts, aligned offsets, slots
+ *   ep_dispatch   : token-major x       -> expert-major rows (bf16 or FP8)
+ *   ep_combine    : expert-major rows   -> token-major y (gate-weighted)
+ *
+ * Sources (page title, section):
+ *  "GPU Microarchitecture: DeepEP from First Principles" -- 1.1 and 1.2
+ *  (dispatch token-major -> destination-major -> expert-major; combine back,
+ *  Output(T0) = 0.73 x Expert2(T0) + 0.27 x Expert7(T0)), 6.1 / 6.2 (layout
+ *  and identity metadata), 7.1 (count -> prefix sum -> scatter).
+ *  "Deep Dive - DeepEP" -- "V2's single interface: ElasticBuffer" (problem
+ *  statement: max tokens, hidden, top-k, FP8 dispatch), "Dispatch: layout,
+ *  move, and epilogue" (topk_idx / topk_weights contract, -1 = unused,
+ *  expanded mode, expert alignment, psum semantics, zero padding, CPU sync),
+ *  "Combine: reverse routing plus reduction" (fp32 accumulation, one bf16
+ *  cast), "Precision: FP8 on the wire, BF16 for the reduction" (one fp32
+ *  scale per 128 values), "EPHandle: route metadata with a lifetime" (the
+ *  handle carries route metadata, not gate values; deterministic order).
+ *
+ * Conventions for every entry point
+ *  - Pointers named d_* or documented "device" are CUDA device pointers; all
+ *    buffers are allocated and owned by the CALLER.  The library never
+ *    allocates, frees or keeps a pointer after a call returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued asynchronously on it; a call returns before
+ *    the GPU has finished unless documented otherwise.
+ *  - Argument errors are detected on the host before anything is launched
+ *    and returned synchronously (EP_ERR_INVALID_ARG).  Errors in the routing
+ *    data (an expert id outside [-1, E), an expert repeated within a token)
+ *    can only be seen on the GPU: they are recorded in the layout's device
+ *    error word and reported by ep_check_error (or by ep_get_layout when it
+ *    is asked to synchronise).  Kernels never trap.
+ *  - Every device pointer must be 16-byte aligned.
+ *  - Row-major layouts throughout.  T = num_tokens of the ep_get_layout call
+ *    (<= cfg.max_tokens), H = hidden, K = num_topk, E = num_experts,
+ *    R = num_ranks, A = expert_alignment, cap = ep_recv_capacity(cfg).
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define EP_API __attribute__((visibility("default")))
+#else
+#define EP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point (int32_t). */
+enum {
+  EP_OK = 0,
+  EP_ERR_INVALID_ARG = 1,   /* bad config, pointer, alignment or size      */
+  EP_ERR_EXPERT_RANGE = 2,  /* a topk_idx entry outside [-1, E)            */
+  EP_ERR_DUP_EXPERT = 3,    /* an expert selected twice by one token       */
+  EP_ERR_CAPACITY = 4,      /* receive buffer smaller than needed          */
+  EP_ERR_CUDA = 5,          /* a CUDA runtime call failed                  */
+  EP_ERR_TIMEOUT = 6        /* a bounded on-chip wait gave up (no hang)    */
+};
+
+/* Problem statement, as in the pages' buffer constructor: max tokens,
+ * hidden size, top-k, expert count, FP8 dispatch; plus the logical rank
+ * count, the expert alignment and the zero-padding switch of dispatch. */
+typedef struct {
+  int32_t max_tokens;        /* tokens a layout may hold (capacity planning)   */
+  int32_t hidden;            /* H: bf16 channels per row; H % 8 == 0, and
+                                H % 128 == 0 when use_fp8_dispatch            */
+  int32_t num_topk;          /* K in [1, 32], K <= E                           */
+  int32_t num_experts;       /* E in [1, 2048]                                  */
+  int32_t num_ranks;         /* R logical ranks, E % R == 0; rank r owns the
+                                experts [r*E/R, (r+1)*E/R)                     */
+  int32_t expert_alignment;  /* A in [1, 1024]: every expert segment starts
+                                at a multiple of A rows                        */
+  int32_t use_fp8_dispatch;  /* 0: bf16 rows; 1: E4M3 rows + 1x128 fp32 scales */
+  int32_t zero_padding;      /* 1: dispatch clears the alignment gap rows      */
+} ep_config;
+
+/* The layout handle: route metadata only (no gate values).  Every pointer is
+ * a caller-allocated DEVICE buffer of the size given; ep_get_layout fills
+ * them and sets num_tokens.  The handle stays valid, and may be reused by
+ * any number of dispatch / combine calls, while the route is unchanged. */
+typedef struct {
+  int32_t *expert_count;     /* [E]   rows routed to each expert (unaligned)   */
+  int32_t *expert_start;     /* [E+1] aligned start row of each expert segment;
+                                expert_start[E] = rows in use                  */
+  int32_t *expert_end;       /* [E]   expert_start[e] + expert_count[e]: the
+                                end of expert e's valid rows (psum semantics)  */
+  int32_t *rank_start;       /* [R+1] first row of each logical rank's range
+                                (= expert_start[r*E/R])                        */
+  int32_t *tokens_per_rank;  /* [R]   tokens sent to each rank, counted once
+                                per (token, rank)                              */
+  uint8_t *is_token_in_rank; /* [max_tokens*R] 1 if token t has an expert
+                                on rank r                                      */
+  int32_t *slot_of;          /* [max_tokens*K] row of (t,k) in the expert-major
+                                buffer, -1 for an unused (-1) selection        */
+  int32_t *src_info;         /* [cap*2] (token, k) of each row in use;
+                                (-1,-1) for alignment padding rows             */
+  int32_t *err;              /* [1]   device error word                        */
+  void *workspace;           /* ep_layout_workspace_bytes(cfg) bytes           */
+  int32_t num_tokens;        /* set by ep_get_layout                           */
+  int32_t reserved;
+} ep_layout;
+
+/* Rows the expert-major buffer needs in the worst case:
+ * max_tokens*K + E*(A-1).  Returns -1 if the config is invalid. */
+EP_API int64_t ep_recv_capacity(const ep_config *cfg);
+
+/* Bytes of device scratch memory ep_get_layout needs in layout->workspace
+ * (per-tile expert histograms and bases).  Returns -1 if the config is
+ * invalid. */
+EP_API int64_t ep_layout_workspace_bytes(const ep_config *cfg);
+
+/* Layout ("GPU Microarchitecture: DeepEP from First Principles", 6.1 and 7.1;
+ * "Deep Dive - DeepEP", "Dispatch: layout, move, and epilogue").
+ *
+ * d_topk_idx: device int64 [num_tokens, K]; -1 marks an unused selection.
+ * Counts rows per expert and per destination rank (a token counts once per
+ * rank), lays the experts out contiguously with every segment rounded up to
+ * A rows, and assigns each (t, k) its row: within an expert, rows follow
+ * source-global order (source rank, token, k) -- the pages' deterministic
+ * mode, produced directly.  Logical source ranks own contiguous token
+ * blocks, so that order is (t, k) order.  Runs three kernels on `stream`.
+ *
+ * h_expert_count: NULL for a fully asynchronous call.  If non-NULL (host
+ * memory, E int32), the call synchronises `stream`, copies the per-expert
+ * counts there and returns the device error status (the pages' CPU-sync
+ * path).  Without it, consumers must use only rows [expert_start[e],
+ * expert_end[e]) and call ep_check_error to see routing errors.
+ * num_tokens may be 0.  Returns EP_OK or an error. */
+EP_API int32_t ep_get_layout(const ep_config *cfg, int32_t num_tokens,
+                      const int64_t *d_topk_idx, ep_layout *layout,
+                      int32_t *h_expert_count, void *stream);
+
+/* Dispatch, expanded mode ("GPU Microarchitecture: DeepEP from First
+ * Principles", 1.1; "Deep Dive - DeepEP", "Dispatch: layout, move, and
+ * epilogue" and "Precision: FP8 on the wire, BF16 for the reduction").
+ *
+ * d_x: device bf16 [T, H] (raw 16-bit patterns).
+ * d_topk_weights: device fp32 [T, K] or NULL.
+ * d_recv_x: device [cap, H]: bf16 rows, or E4M3 bytes when use_fp8_dispatch.
+ *   Row slot_of[t,k] receives token t.  bf16 rows are bit copies.  FP8 rows:
+ *   per 128-channel block, amax = max|x| (exact), scale = amax / 448 (fp32,
+ *   round to nearest), q = E4M3(x / scale) rounded to nearest even with
+ *   saturation to +-448; an all-zero block has scale 0 and q = 0.
+ * d_recv_scale: device fp32 [cap, H/128] (FP8 only, else ignored; may be
+ *   NULL for bf16): the dequantisation multipliers, x ~ q * scale.
+ * d_recv_w: device fp32 [cap] or NULL: recv_w[slot_of[t,k]] = w[t,k], one
+ *   gate weight per expert row (requires d_topk_weights).
+ * With cfg->zero_padding, rows [expert_end[e], expert_start[e+1]) get
+ * zero payload, zero scales and zero weight.  Rows at or past
+ * expert_start[E] are never written.  Returns EP_OK or an error. */
+EP_API int32_t ep_dispatch(const ep_config *cfg, const ep_layout *layout,
+                    const void *d_x, const float *d_topk_weights,
+                    void *d_recv_x, float *d_recv_scale, float *d_recv_w,
+                    void *stream);
+
+/* Combine ("GPU Microarchitecture: DeepEP from First Principles", 1.2;
+ * "Deep Dive - DeepEP", "Combine: reverse routing plus reduction").
+ *
+ * d_expert_out: device bf16 [cap, H] in the layout's row order (the expert
+ *   outputs of the dispatched rows).
+ * d_topk_weights: device fp32 [T, K], or NULL.  For each token and channel,
+ *   acc = +0.0f; for k = 0..K-1 with slot_of[t,k] >= 0:
+ *   acc = fmaf(w[t,k], expert_out[slot_of[t,k], i], acc); y = bf16(acc),
+ *   round to nearest even.  Each gate weight is applied exactly once; with
+ *   NULL every weight is 1, i.e. the plain sum of rows the caller already
+ *   weighted (the pages' V2 contract).  Unused selections contribute
+ *   nothing and the remaining weights are not renormalised; padding rows
+ *   are never read.
+ * d_y: device bf16 [T, H].  Returns EP_OK or an error. */
+EP_API int32_t ep_combine(const ep_config *cfg, const ep_layout *layout,
+                   const void *d_expert_out, const float *d_topk_weights,
+                   void *d_y, void *stream);
+
+/* Synchronises `stream` and returns the status recorded in the layout's
+ * device error word (EP_OK if none): routing errors found by ep_get_layout,
+ * and EP_ERR_TIMEOUT if a bounded on-chip wait of a later call gave up. */
+EP_API int32_t ep_check_error(const ep_layout *layout, void *stream);
+
+/* Self-test of the bounded on-chip wait used by the pipelined kernels:
+ * launches one CTA that waits on a shared-memory barrier nothing will ever
+ * complete, with a limit of timeout_ns nanoseconds.  The wait gives up, the
+ * kernel records EP_ERR_TIMEOUT in d_err (device int32, OR-ed in) and
+ * returns; the GPU context stays usable.  Synchronises `stream` and returns
+ * the recorded status (EP_ERR_TIMEOUT when the mechanism works).
+ * timeout_ns must be in [1000, 10^9]. */
+EP_API int32_t ep_selftest_wait_timeout(int64_t timeout_ns, int32_t *d_err,
+                                        void *stream);
+
+/* Static, human-readable name of a status code. */
+EP_API const char *ep_status_str(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EP_GB300_H */

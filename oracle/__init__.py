@@ -166,8 +166,10 @@ def layout(topk_idx: np.ndarray, num_experts: int, num_ranks: int,
     return out
 
 
-def dispatch_bf16(x, topk_weights, lay: dict, zero_padding=False, fill=0xFFFF):
-    """Expanded bf16 dispatch; rows the method does not write keep ``fill``."""
+def dispatch_bf16(x, topk_weights, lay: dict, zero_padding=False, fill=0xFFFF,
+                  out=None):
+    """Expanded bf16 dispatch; rows the method does not write keep ``fill``
+    (or their previous contents when ``out=(recv_x, recv_w)`` is given)."""
     x = _c(x, np.uint16)
     T, H = x.shape
     slot_of = _c(lay["slot_of"], np.int32)
@@ -175,8 +177,13 @@ def dispatch_bf16(x, topk_weights, lay: dict, zero_padding=False, fill=0xFFFF):
     E = lay["expert_count"].shape[0]
     cap = lay["cap"]
     w = None if topk_weights is None else _c(topk_weights, np.float32)
-    recv_x = np.full((cap, H), fill, np.uint16)
-    recv_w = np.full(cap, np.nan, np.float32)
+    if out is not None:
+        recv_x, recv_w = out
+        assert recv_x.shape == (cap, H) and recv_x.dtype == np.uint16
+        assert recv_w.shape == (cap,) and recv_w.dtype == np.float32
+    else:
+        recv_x = np.full((cap, H), fill, np.uint16)
+        recv_w = np.full(cap, np.nan, np.float32)
     lib().oracle_dispatch_bf16(T, H, K, E, _ptr(x), _ptr(w), _ptr(slot_of),
                                _ptr(_c(lay["expert_start"], np.int32)),
                                _ptr(_c(lay["expert_end"], np.int32)),
@@ -204,14 +211,18 @@ def dispatch_fp8(x, topk_weights, lay: dict, zero_padding=False, fill=0xFF):
     return recv_q, recv_scale, recv_w
 
 
-def combine(expert_out, topk_weights, slot_of) -> np.ndarray:
+def combine(expert_out, topk_weights, slot_of, out=None) -> np.ndarray:
     """Combine from the definition: returns y (uint16 bf16 bits [T, H])."""
     Y = _c(expert_out, np.uint16)
     H = Y.shape[1]
     slot_of = _c(slot_of, np.int32)
     T, K = slot_of.shape
     w = None if topk_weights is None else _c(topk_weights, np.float32)
-    y = np.zeros((T, H), np.uint16)
+    if out is not None:
+        y = out
+        assert y.shape == (T, H) and y.dtype == np.uint16
+    else:
+        y = np.zeros((T, H), np.uint16)
     lib().oracle_combine(T, H, K, _ptr(Y), _ptr(w), _ptr(slot_of), _ptr(y))
     return y
 

@@ -10,6 +10,17 @@ if ROOT not in sys.path:
 GOLDEN = os.path.join(ROOT, "tests", "golden")
 
 
+def load_build_module():
+    """The library's standalone build script, loaded by path."""
+    import importlib.util
+
+    path = os.path.join(ROOT, "combine_get_layout_gb300", "build_lib.py")
+    spec = importlib.util.spec_from_file_location("ep_build_lib", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
 
