@@ -2,7 +2,7 @@
 """Benchmark of the MoE dispatch / combine layout path on GB300.
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-layout (3 kernels) -> dispatch -> combine, through the library's C ABI.
+layout (2 kernels) -> dispatch -> combine, through the library's C ABI.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload prefill]
   python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
@@ -207,6 +207,13 @@ def barrier(world: int):
         import torch.distributed as dist
 
         dist.barrier()
+
+
+def job_throughput(tokens_per_rank: int, ms_local: float, world: int, device=None):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's step
+    time.  Returns (value, ms_max)."""
+    ms = reduce_max(ms_local, world, device)
+    return tokens_per_rank * world / (ms / 1e3), ms
 
 
 # ---------------------------------------------------------------------------
@@ -414,7 +421,10 @@ def run_ours(args):
         st = ep.ep_combine(ccfg, L.c, p(Y), p(w_d), p(out), sptr)
         assert st == 0, ep.ep_status_str(st)
 
-    launches_per_step = (3 if T > 0 else 1) + 1 + (1 if args.zero_padding else 0) + (1 if T > 0 else 0)
+    # layout: count + assign (assign alone when T == 0); dispatch (+ padding);
+    # combine
+    launches_per_step = (2 if T > 0 else 1) + (1 if T > 0 else 0) + \
+        (1 if args.zero_padding else 0) + (1 if T > 0 else 0)
 
     # ---- device-resident timing ---------------------------------------------
     dev_id = str(local)
@@ -449,8 +459,7 @@ def run_ours(args):
     com_ms = [e[2].elapsed_time(e[3]) for e in ev]
     step_ms = [e[0].elapsed_time(e[3]) for e in ev]
     ms_local = statistics.mean(step_ms)
-    ms = reduce_max(ms_local, world, device)
-    value = T * world / (ms / 1e3)
+    value, ms = job_throughput(T, ms_local, world, device)
 
     peak, peak_src = load_peaks()
     b = algorithmic_bytes(wl, n_rows)
@@ -544,7 +553,7 @@ def run_ours(args):
             "dtype": "bf16", "data": "synthetic (seeded router simulation, PCG64; no dataset)",
             "config": workload_config(wl, extra={
                 "l2": "flushed before every step (256 MiB write), outside the step events",
-                "step": "layout (3 kernels) + dispatch + combine; combine reads a "
+                "step": "layout (2 kernels) + dispatch + combine; combine reads a "
                         "device-resident seeded N(0,1) expert-output buffer",
                 "parallelism": f"{world} independent replica(s)",
                 "zero_padding": bool(args.zero_padding)}),

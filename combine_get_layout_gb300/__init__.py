@@ -41,6 +41,7 @@ ABI_SYMBOLS = (
     "ep_combine",
     "ep_check_error",
     "ep_selftest_wait_timeout",
+    "ep_last_cuda_error",
     "ep_status_str",
 )
 
@@ -97,6 +98,8 @@ def _load():
     L.ep_check_error.argtypes = [P(EpLayout), vp]
     L.ep_selftest_wait_timeout.restype = i32
     L.ep_selftest_wait_timeout.argtypes = [i64, vp, vp]
+    L.ep_last_cuda_error.restype = i32
+    L.ep_last_cuda_error.argtypes = []
     L.ep_status_str.restype = ctypes.c_char_p
     L.ep_status_str.argtypes = [i32]
     return L
@@ -145,6 +148,10 @@ def ep_selftest_wait_timeout(timeout_ns, d_err, stream) -> int:
     return int(_lib.ep_selftest_wait_timeout(int(timeout_ns), d_err, stream))
 
 
+def ep_last_cuda_error() -> int:
+    return int(_lib.ep_last_cuda_error())
+
+
 def ep_status_str(status: int) -> str:
     return _lib.ep_status_str(int(status)).decode()
 
@@ -154,7 +161,11 @@ def ep_status_str(status: int) -> str:
 class EpError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         self.status = int(status)
-        super().__init__(f"{what}: {ep_status_str(status)} ({status})")
+        msg = f"{what}: {ep_status_str(status)} ({status})"
+        if self.status == EP_ERR_CUDA:
+            self.cuda_error = ep_last_cuda_error()
+            msg += f", cudaError {self.cuda_error}"
+        super().__init__(msg)
 
 
 def _check(status: int, what: str):

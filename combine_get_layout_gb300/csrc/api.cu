@@ -30,6 +30,28 @@ const DeviceInfo& device_info() {
   return infos[dev];
 }
 
+static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+cudaError_t note_cuda(cudaError_t e) {
+  if (e != cudaSuccess) g_last_cuda_error = e;
+  return e;
+}
+
+// One-time per-device kernel set-up (shared-memory limits).
+static cudaError_t ensure_prepared() {
+  static std::once_flag once[kMaxDevices];
+  static cudaError_t result[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  std::call_once(once[dev], [dev] {
+    (void)device_info();
+    cudaError_t e = prepare_layout_kernels();
+    if (e == cudaSuccess) e = prepare_dispatch_kernels();
+    result[dev] = e;
+  });
+  return note_cuda(result[dev]);
+}
+
 static bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
@@ -62,7 +84,7 @@ static int64_t capacity(const ep_config* c) {
 }
 
 static int32_t cuda_status(cudaError_t e) {
-  return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+  return note_cuda(e) == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 
 static int32_t status_from_bits(int32_t bits) {
@@ -94,8 +116,7 @@ int64_t ep_recv_capacity(const ep_config* cfg) {
 
 int64_t ep_layout_workspace_bytes(const ep_config* cfg) {
   if (!config_ok(cfg)) return -1;
-  const int tiles = layout_max_tiles(cfg->max_tokens, cfg->num_topk);
-  return layout_workspace_bytes(tiles, cfg->num_experts, cfg->num_ranks);
+  return layout_workspace_bytes(cfg->num_experts, cfg->num_ranks);
 }
 
 int32_t ep_get_layout(const ep_config* cfg, int32_t num_tokens,
@@ -106,7 +127,7 @@ int32_t ep_get_layout(const ep_config* cfg, int32_t num_tokens,
   if (num_tokens > 0 && (d_topk_idx == nullptr || !aligned16(d_topk_idx)))
     return EP_ERR_INVALID_ARG;
   const int K = cfg->num_topk, E = cfg->num_experts, R = cfg->num_ranks;
-  const int max_tiles = layout_max_tiles(cfg->max_tokens, K);
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
   LayoutArgs a;
   a.topk_idx = d_topk_idx;
   a.T = num_tokens;
@@ -115,8 +136,8 @@ int32_t ep_get_layout(const ep_config* cfg, int32_t num_tokens,
   a.R = R;
   a.A = cfg->expert_alignment;
   a.geom = layout_tiles(num_tokens > 0 ? num_tokens : 1, K);
-  if (a.geom.num_tiles > max_tiles) return EP_ERR_INVALID_ARG;
-  a.ws = carve_layout_workspace(layout->workspace, max_tiles, E, R);
+  if (a.geom.num_tiles > kLayoutMaxTiles) return EP_ERR_INVALID_ARG;
+  a.ws = carve_layout_workspace(layout->workspace, E, R);
   a.expert_count = layout->expert_count;
   a.expert_start = layout->expert_start;
   a.expert_end = layout->expert_end;
@@ -127,7 +148,7 @@ int32_t ep_get_layout(const ep_config* cfg, int32_t num_tokens,
   a.err = layout->err;
   a.is_token_in_rank = layout->is_token_in_rank;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_layout(a, s);
+  cudaError_t e = note_cuda(launch_layout(a, s));
   if (e != cudaSuccess) return EP_ERR_CUDA;
   layout->num_tokens = num_tokens;
   if (h_expert_count != nullptr) {
@@ -137,7 +158,7 @@ int32_t ep_get_layout(const ep_config* cfg, int32_t num_tokens,
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(&bits, layout->err, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return EP_ERR_CUDA;
+    if (note_cuda(e) != cudaSuccess) return EP_ERR_CUDA;
     return status_from_bits(bits);
   }
   return EP_OK;
@@ -157,6 +178,7 @@ int32_t ep_dispatch(const ep_config* cfg, const ep_layout* layout,
   if (d_recv_w != nullptr && d_topk_weights == nullptr) return EP_ERR_INVALID_ARG;
   if (cfg->use_fp8_dispatch && (d_recv_scale == nullptr || !aligned16(d_recv_scale)))
     return EP_ERR_INVALID_ARG;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
   DispatchArgs a;
   a.x = d_x;
   a.topk_weights = d_topk_weights;
@@ -187,6 +209,7 @@ int32_t ep_combine(const ep_config* cfg, const ep_layout* layout,
     if (d_y == nullptr || !aligned16(d_y)) return EP_ERR_INVALID_ARG;
   }
   if (d_topk_weights != nullptr && !aligned16(d_topk_weights)) return EP_ERR_INVALID_ARG;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
   CombineArgs a;
   a.expert_out = d_expert_out;
   a.topk_weights = d_topk_weights;
@@ -205,7 +228,7 @@ int32_t ep_check_error(const ep_layout* layout, void* stream) {
   cudaError_t e = cudaMemcpyAsync(&bits, layout->err, sizeof(int32_t),
                                   cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return EP_ERR_CUDA;
+  if (note_cuda(e) != cudaSuccess) return EP_ERR_CUDA;
   return status_from_bits(bits);
 }
 
@@ -218,8 +241,14 @@ int32_t ep_selftest_wait_timeout(int64_t timeout_ns, int32_t* d_err, void* strea
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(&bits, d_err, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return EP_ERR_CUDA;
+  if (note_cuda(e) != cudaSuccess) return EP_ERR_CUDA;
   return status_from_bits(bits);
+}
+
+int32_t ep_last_cuda_error(void) {
+  const cudaError_t e = g_last_cuda_error;
+  g_last_cuda_error = cudaSuccess;
+  return static_cast<int32_t>(e);
 }
 
 const char* ep_status_str(int32_t status) {

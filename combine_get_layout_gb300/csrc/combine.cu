@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(256)
   const int t = blockIdx.x;
   const int tid = threadIdx.x;
   const int nvec = H >> 3;
+  pdl_wait();
+  pdl_launch_dependents();
   if (tid < K) {
     s_slot[tid] = slot_of[int64_t(t) * K + tid];
     s_w[tid] = w != nullptr ? w[int64_t(t) * K + tid] : 1.0f;
@@ -73,10 +75,9 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
   const int nvec = a.H / 8;
   const int threads = nvec >= 128 ? 128 : ((nvec + 31) / 32) * 32;
-  combine_kernel<<<a.T, threads, 0, stream>>>(
-      static_cast<const uint4*>(a.expert_out), a.topk_weights, a.slot_of, a.H,
-      a.K, static_cast<uint4*>(a.y));
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(a.T), dim3(threads), 0, stream,
+                    static_cast<const uint4*>(a.expert_out), a.topk_weights,
+                    a.slot_of, a.H, a.K, static_cast<uint4*>(a.y));
 }
 
 }  // namespace ep

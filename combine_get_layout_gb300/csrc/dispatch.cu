@@ -39,13 +39,19 @@ __global__ void __launch_bounds__(32)
   const int n = T > static_cast<int>(blockIdx.x)
                     ? (T - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
                     : 0;
-  if (n == 0) return;
+  if (n == 0) {
+    pdl_wait();
+    pdl_launch_dependents();
+    return;
+  }
 
   if (lane == 0) {
     for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
   }
   __syncwarp();
+  pdl_wait();
+  pdl_launch_dependents();
 
   auto token = [&](int i) { return static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x); };
   auto issue = [&](int i) {  // lane 0 only
@@ -123,6 +129,8 @@ __global__ void __launch_bounds__(1024)
   const int tid = threadIdx.x;
   const int nvec = H >> 3;     // 16-byte vectors (8 channels) per row
   const int nblk = H >> 7;     // 128-channel scale blocks per row
+  pdl_wait();
+  pdl_launch_dependents();
   if (tid < K) {
     const int sl = slot_of[int64_t(t) * K + tid];
     s_slot[tid] = sl;
@@ -183,6 +191,8 @@ __global__ void __launch_bounds__(256)
                         uint8_t* __restrict__ recv_x,
                         float* __restrict__ recv_scale,
                         float* __restrict__ recv_w) {
+  pdl_wait();
+  pdl_launch_dependents();
   for (int e = blockIdx.x; e < E; e += gridDim.x) {
     const int64_t s0 = expert_end[e], s1 = expert_start[e + 1];
     if (s1 <= s0) continue;
@@ -200,6 +210,8 @@ __global__ void __launch_bounds__(256)
 // Self-test of mbar_wait: the barrier expects one arrival that never comes.
 __global__ void __launch_bounds__(32) wait_selftest_kernel(uint64_t timeout_ns, int32_t* err) {
   __shared__ __align__(8) uint64_t bar;
+  pdl_wait();
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
@@ -208,8 +220,28 @@ __global__ void __launch_bounds__(32) wait_selftest_kernel(uint64_t timeout_ns, 
 }
 
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, int32_t* err, cudaStream_t stream) {
-  wait_selftest_kernel<<<1, 32, 0, stream>>>(timeout_ns, err);
-  return cudaGetLastError();
+  return launch_pdl(wait_selftest_kernel, dim3(1), dim3(32), 0, stream, timeout_ns, err);
+}
+
+cudaError_t prepare_dispatch_kernels() {
+  return allow_max_dynamic_smem(dispatch_bf16_kernel, device_info().max_smem_optin);
+}
+
+// CTAs of the bf16 kernel resident per SM for a given shared-memory size
+// (cached: the last query per thread).
+static int bf16_ctas_per_sm(int smem) {
+  thread_local int last_dev = -1, last_smem = -1, last_val = 1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev == last_dev && smem == last_smem) return last_val;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_bf16_kernel, 32,
+                                                    smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  last_dev = dev;
+  last_smem = smem;
+  last_val = per_sm;
+  return per_sm;
 }
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
@@ -221,36 +253,29 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
       if (stages > kMaxStages) stages = kMaxStages;
       if (stages < 2) stages = 2;
       const int smem = kBarrierBytes + stages * int(row_bytes);
-      st = cudaFuncSetAttribute(dispatch_bf16_kernel,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (st != cudaSuccess) return st;
-      int per_sm = 0;
-      st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_bf16_kernel,
-                                                         32, smem);
-      if (st != cudaSuccess) return st;
-      if (per_sm < 1) per_sm = 1;
-      int grid = device_info().sm_count * per_sm;
+      int grid = device_info().sm_count * bf16_ctas_per_sm(smem);
       if (grid > a.T) grid = a.T;
-      dispatch_bf16_kernel<<<grid, 32, smem, stream>>>(
-          static_cast<const uint8_t*>(a.x), a.topk_weights, a.slot_of, a.T, a.K,
-          row_bytes, stages, static_cast<uint8_t*>(a.recv_x), a.recv_w, a.err);
+      st = launch_pdl(dispatch_bf16_kernel, dim3(grid), dim3(32), smem, stream,
+                      static_cast<const uint8_t*>(a.x), a.topk_weights, a.slot_of,
+                      a.T, a.K, row_bytes, stages, static_cast<uint8_t*>(a.recv_x),
+                      a.recv_w, a.err);
     } else {
       const int nvec = a.H / 8;
       int threads = nvec < 1024 ? ((nvec + 31) / 32) * 32 : 1024;
-      dispatch_fp8_kernel<<<a.T, threads, 0, stream>>>(
-          static_cast<const uint4*>(a.x), a.topk_weights, a.slot_of, a.T, a.H,
-          a.K, static_cast<uint8_t*>(a.recv_x), a.recv_scale, a.recv_w);
+      st = launch_pdl(dispatch_fp8_kernel, dim3(a.T), dim3(threads), 0, stream,
+                      static_cast<const uint4*>(a.x), a.topk_weights, a.slot_of,
+                      a.T, a.H, a.K, static_cast<uint8_t*>(a.recv_x), a.recv_scale,
+                      a.recv_w);
     }
-    st = cudaGetLastError();
     if (st != cudaSuccess) return st;
   }
   if (a.zero_padding) {
     const int64_t row_bytes = a.fp8 ? int64_t(a.H) : int64_t(a.H) * 2;
     int grid = a.E < 1024 ? a.E : 1024;
-    zero_padding_kernel<<<grid, 256, 0, stream>>>(
-        a.expert_start, a.expert_end, a.E, row_bytes, a.fp8 ? a.H / 128 : 0,
-        static_cast<uint8_t*>(a.recv_x), a.fp8 ? a.recv_scale : nullptr, a.recv_w);
-    st = cudaGetLastError();
+    st = launch_pdl(zero_padding_kernel, dim3(grid), dim3(256), 0, stream,
+                    a.expert_start, a.expert_end, a.E, row_bytes,
+                    a.fp8 ? a.H / 128 : 0, static_cast<uint8_t*>(a.recv_x),
+                    a.fp8 ? a.recv_scale : nullptr, a.recv_w);
     if (st != cudaSuccess) return st;
   }
   return cudaSuccess;

@@ -35,6 +35,22 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
+// ---- programmatic dependent launch ----------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialisation.  It waits for the preceding grid (griddepcontrol.wait)
+// before its first read of global memory that another kernel may have
+// written, and only after that wait lets the next grid start launching, so
+// that when a kernel of this library passes its own wait, every grid before
+// its predecessor has completed as well.
+
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier -----------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

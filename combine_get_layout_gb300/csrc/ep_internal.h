@@ -5,16 +5,21 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace ep {
 
 // Layout tiling: a tile is a run of whole tokens handled by one CTA of
-// kLayoutThreads threads.  Tiles are sized so that about kLayoutTargetTiles
-// CTAs run, each with between kMinTilePairs and kMaxTilePairs (t, k) pairs.
+// kLayoutThreads threads.  There are at most kLayoutMaxTiles tiles, each of
+// at least kMinTilePairs (t, k) pairs when the input allows.
 constexpr int kLayoutThreads = 256;
 constexpr int kLayoutWarps = kLayoutThreads / 32;
-constexpr int kLayoutTargetTiles = 152;
+constexpr int kLayoutMaxTiles = 152;
 constexpr int kMinTilePairs = 256;
-constexpr int kMaxTilePairs = 4096;
+// Tokens whose destination ranks the count kernel stages at a time.
+constexpr int kRankSubTokens = 256;
+// int32 entries per shared-memory buffer when streaming the tile counts.
+constexpr int kScanChunkInts = 8192;
 
 struct TileGeom {
   int tile_tokens;  // tokens per tile (last tile may be short)
@@ -23,20 +28,21 @@ struct TileGeom {
 
 // Geometry for T tokens of K selections each (T >= 1).
 TileGeom layout_tiles(int64_t T, int K);
-// Largest tile count any T <= max_tokens can produce.
-int layout_max_tiles(int64_t max_tokens, int K);
+
+// Experts padded to a multiple of 4 (rows of the tile-count matrix are then
+// 16-byte multiples, as bulk copies need).
+__host__ __device__ inline int padded_experts(int E) { return (E + 3) & ~3; }
 
 // Workspace carved by ep_get_layout (int32 arrays, each 16-byte aligned):
-//   tile_counts [tiles * E], tile_base [tiles * E],
-//   tile_rank_counts [tiles * R], tile_err [tiles].
+//   tile_counts [kLayoutMaxTiles * Epad], tile_rank_counts
+//   [kLayoutMaxTiles * R], tile_err [kLayoutMaxTiles].
 struct LayoutWorkspace {
   int32_t* tile_counts;
-  int32_t* tile_base;
   int32_t* tile_rank_counts;
   int32_t* tile_err;
 };
-int64_t layout_workspace_bytes(int max_tiles, int E, int R);
-LayoutWorkspace carve_layout_workspace(void* base, int max_tiles, int E, int R);
+int64_t layout_workspace_bytes(int E, int R);
+LayoutWorkspace carve_layout_workspace(void* base, int E, int R);
 
 struct LayoutArgs {
   const int64_t* topk_idx;
@@ -79,6 +85,42 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 
 // One CTA waiting (bounded) on a barrier nothing completes.
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, int32_t* err, cudaStream_t stream);
+
+// Launches `kernel` with programmatic stream serialisation (see pdl_wait in
+// ep_device.cuh).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block,
+                       size_t smem, cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Raises `kernel`'s dynamic shared-memory limit to what the device allows
+// next to the kernel's static shared memory.
+template <typename... Params>
+cudaError_t allow_max_dynamic_smem(void (*kernel)(Params...), int optin) {
+  cudaFuncAttributes fa;
+  cudaError_t st = cudaFuncGetAttributes(&fa, kernel);
+  if (st != cudaSuccess) return st;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              optin - static_cast<int>(fa.sharedSizeBytes));
+}
+
+// Records a failed CUDA runtime status for ep_last_cuda_error (per thread).
+cudaError_t note_cuda(cudaError_t e);
+
+// Per-device one-time set-up of the kernels' shared-memory limits.
+cudaError_t prepare_layout_kernels();
+cudaError_t prepare_dispatch_kernels();
 
 // Cached per-device properties (queried once per device).
 struct DeviceInfo {

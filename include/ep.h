@@ -198,6 +198,11 @@ EP_API int32_t ep_check_error(const ep_layout *layout, void *stream);
 EP_API int32_t ep_selftest_wait_timeout(int64_t timeout_ns, int32_t *d_err,
                                         void *stream);
 
+/* The cudaError_t of the last CUDA runtime call of this library that failed
+ * in the calling thread (0 if none since the previous query); reading it
+ * clears it.  Explains an EP_ERR_CUDA status. */
+EP_API int32_t ep_last_cuda_error(void);
+
 /* Static, human-readable name of a status code. */
 EP_API const char *ep_status_str(int32_t status);
 
