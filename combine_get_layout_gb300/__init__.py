@@ -42,6 +42,7 @@ ABI_SYMBOLS = (
     "ep_check_error",
     "ep_selftest_wait_timeout",
     "ep_last_cuda_error",
+    "ep_get_layout_noalloc",
     "ep_status_str",
 )
 
@@ -98,6 +99,8 @@ def _load():
     L.ep_check_error.argtypes = [P(EpLayout), vp]
     L.ep_selftest_wait_timeout.restype = i32
     L.ep_selftest_wait_timeout.argtypes = [i64, vp, vp]
+    L.ep_get_layout_noalloc.restype = i32
+    L.ep_get_layout_noalloc.argtypes = [P(EpConfig), i32, vp, P(EpLayout), vp, vp]
     L.ep_last_cuda_error.restype = i32
     L.ep_last_cuda_error.argtypes = []
     L.ep_status_str.restype = ctypes.c_char_p
@@ -146,6 +149,15 @@ def ep_check_error(layout, stream) -> int:
 
 def ep_selftest_wait_timeout(timeout_ns, d_err, stream) -> int:
     return int(_lib.ep_selftest_wait_timeout(int(timeout_ns), d_err, stream))
+
+
+def ep_get_layout_noalloc(cfg, num_tokens, d_topk_idx, layout, h_expert_count,
+                          stream) -> int:
+    """ep_get_layout with the scratch in the library's own device memory
+    (layout.workspace is ignored)."""
+    return int(_lib.ep_get_layout_noalloc(ctypes.byref(cfg), num_tokens, d_topk_idx,
+                                          ctypes.byref(layout), h_expert_count,
+                                          stream))
 
 
 def ep_last_cuda_error() -> int:

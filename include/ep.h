@@ -64,7 +64,7 @@ enum {
   EP_ERR_INVALID_ARG = 1,   /* bad config, pointer, alignment or size      */
   EP_ERR_EXPERT_RANGE = 2,  /* a topk_idx entry outside [-1, E)            */
   EP_ERR_DUP_EXPERT = 3,    /* an expert selected twice by one token       */
-  EP_ERR_CAPACITY = 4,      /* receive buffer smaller than needed          */
+  EP_ERR_CAPACITY = 4,      /* a buffer or built-in scratch is too small   */
   EP_ERR_CUDA = 5,          /* a CUDA runtime call failed                  */
   EP_ERR_TIMEOUT = 6        /* a bounded on-chip wait gave up (no hang)    */
 };
@@ -182,6 +182,33 @@ EP_API int32_t ep_dispatch(const ep_config *cfg, const ep_layout *layout,
 EP_API int32_t ep_combine(const ep_config *cfg, const ep_layout *layout,
                    const void *d_expert_out, const float *d_topk_weights,
                    void *d_y, void *stream);
+
+/* Allocation-free layout.  The pages have no counterpart: this entry point
+ * exists for callers that cannot allocate device memory -- code inside a
+ * framework that owns all device memory and has no spare buffer to give, a
+ * serving loop that must not allocate after warm-up (cudaMalloc can
+ * synchronise the device and fragment a sized pool), or a plugin that only
+ * receives the tensors it computes on.
+ *
+ * Same arguments and results as ep_get_layout, except that
+ * layout->workspace is ignored (it may be NULL): the per-tile scratch lives
+ * in a 1 MiB array in the library's own device memory, which every GPU that
+ * loads the library holds until the process exits.  Configurations whose
+ * ep_layout_workspace_bytes exceeds 1 MiB (152 * 4 * (E rounded up to 4,
+ * plus R, plus 1) bytes, roughly) are rejected with EP_ERR_CAPACITY before
+ * anything is launched.  Nothing is allocated or freed, by this call or by
+ * any routine it calls.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any
+ * stream capture.  All calls share the one array and it keeps the last
+ * call's contents; every call writes the scratch it reads before reading
+ * it, so nothing has to start at zero.  Calls whose work overlaps on the GPU
+ * (e.g. on two streams at once) race on the array: order them. */
+EP_API int32_t ep_get_layout_noalloc(const ep_config *cfg, int32_t num_tokens,
+                                     const int64_t *d_topk_idx,
+                                     ep_layout *layout,
+                                     int32_t *h_expert_count, void *stream);
 
 /* Synchronises `stream` and returns the status recorded in the layout's
  * device error word (EP_OK if none): routing errors found by ep_get_layout,
