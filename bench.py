@@ -12,7 +12,9 @@ Prints ONE JSON line on rank 0.  Everything else goes to stderr.
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
 and torch.cuda.synchronize() on both sides.  Each step is timed on the
 launching stream with CUDA events (one pair per kernel group), and the L2 is
-flushed (a 256 MiB write) before every step, outside the events; the reported
+flushed before every step, outside the events: a 256 MiB write evicts the
+workload's lines, then a 256 MiB read evicts the write's dirty lines, so that
+no step pays for write-backs of the flush itself; the reported
 ms_per_step is the mean step time, maximum over ranks.  With N > 1 (torchrun)
 every rank runs an independent replica of the workload (weak scaling; the
 path has no cross-rank step on a single-GPU-per-problem layout).
@@ -39,7 +41,7 @@ METRIC = ("dispatch+combine tokens/s and HBM GB/s (% of 8 TB/s) at DeepSeek-V3 "
           "shape, 1 GB300")
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-L2_FLUSH_BYTES = 256 << 20
+L2_FLUSH_BYTES = 256 << 20  # twice the GB300's L2
 
 
 def log(*a):
@@ -59,6 +61,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=12.0)
+    p.add_argument("--graph", action="store_true",
+                   help="replay each kernel group from a captured CUDA graph "
+                        "(removes host launch overhead; for latency-bound sizes)")
     return p.parse_args()
 
 
@@ -404,27 +409,54 @@ def run_ours(args):
               if wl.use_fp8_dispatch else None)
     recv_w = torch.empty(cap, dtype=torch.float32, device=device)
     y_d = torch.empty((T, H), dtype=torch.bfloat16, device=device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+
+    def l2_flush():
+        flush_w.zero_()
+        flush_r.sum()
     stream = torch.cuda.current_stream(device)
     sptr = ctypes.c_void_p(stream.cuda_stream)
+    fn_stream = [sptr]  # the stream the library calls below launch on
     p = lambda t: None if t is None else t.data_ptr()
 
     def layout():
-        st = ep.ep_get_layout(ccfg, T, p(idx_d), L.c, None, sptr)
+        st = ep.ep_get_layout(ccfg, T, p(idx_d), L.c, None, fn_stream[0])
         assert st == 0, ep.ep_status_str(st)
 
     def dispatch(xsrc):
-        st = ep.ep_dispatch(ccfg, L.c, p(xsrc), p(w_d), p(recv_x), p(recv_s), p(recv_w), sptr)
+        st = ep.ep_dispatch(ccfg, L.c, p(xsrc), p(w_d), p(recv_x), p(recv_s), p(recv_w),
+                            fn_stream[0])
         assert st == 0, ep.ep_status_str(st)
 
     def combine(Y, out):
-        st = ep.ep_combine(ccfg, L.c, p(Y), p(w_d), p(out), sptr)
+        st = ep.ep_combine(ccfg, L.c, p(Y), p(w_d), p(out), fn_stream[0])
         assert st == 0, ep.ep_status_str(st)
 
     # layout: count + assign (assign alone when T == 0); dispatch (+ padding);
     # combine
     launches_per_step = (2 if T > 0 else 1) + (1 if T > 0 else 0) + \
         (1 if args.zero_padding else 0) + (1 if T > 0 else 0)
+
+    run_layout, run_dispatch, run_combine = layout, lambda: dispatch(x_d), lambda: combine(Y_d, y_d)
+    if args.graph:
+        # warm up (one-time per-device set-up happens outside any capture)
+        run_layout(); run_dispatch(); run_combine()
+        torch.cuda.synchronize()
+        graphs = []
+        for fn in (run_layout, run_dispatch, run_combine):
+            g_ = torch.cuda.CUDAGraph()
+            cap_stream = torch.cuda.Stream(device)
+            cap_stream.wait_stream(stream)
+            with torch.cuda.graph(g_, stream=cap_stream):
+                st_ptr = ctypes.c_void_p(cap_stream.cuda_stream)
+                fn_stream[0] = st_ptr
+                fn()
+                fn_stream[0] = sptr
+            graphs.append(g_)
+        torch.cuda.synchronize()
+        run_layout, run_dispatch, run_combine = (graphs[0].replay, graphs[1].replay,
+                                                 graphs[2].replay)
 
     # ---- device-resident timing ---------------------------------------------
     dev_id = str(local)
@@ -434,8 +466,8 @@ def run_ours(args):
         pass
     sampler = ClockSampler(dev_id)
     for _ in range(args.warmup):
-        flush.zero_()
-        layout(); dispatch(x_d); combine(Y_d, y_d)
+        l2_flush()
+        run_layout(); run_dispatch(); run_combine()
     torch.cuda.synchronize()
     assert ep.ep_check_error(L.c, sptr) == 0
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
@@ -443,11 +475,11 @@ def run_ours(args):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(args.steps):
-        flush.zero_()
+        l2_flush()
         e = ev[i]
-        e[0].record(stream); layout()
-        e[1].record(stream); dispatch(x_d)
-        e[2].record(stream); combine(Y_d, y_d)
+        e[0].record(stream); run_layout()
+        e[1].record(stream); run_dispatch()
+        e[2].record(stream); run_combine()
         e[3].record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -520,14 +552,14 @@ def run_ours(args):
             y_h.copy_(y_d, non_blocking=True)
 
         for _ in range(args.warmup):
-            flush.zero_()
+            l2_flush()
             e2e_step()
         torch.cuda.synchronize()
         eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
         barrier(world)
         torch.cuda.synchronize()
         for i in range(args.steps):
-            flush.zero_()
+            l2_flush()
             eev[i][0].record(stream)
             e2e_step()
             eev[i][1].record(stream)
@@ -552,10 +584,12 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded router simulation, PCG64; no dataset)",
             "config": workload_config(wl, extra={
-                "l2": "flushed before every step (256 MiB write), outside the step events",
+                "l2": "flushed before every step (256 MiB write, then 256 MiB read), outside the step events",
                 "step": "layout (2 kernels) + dispatch + combine; combine reads a "
                         "device-resident seeded N(0,1) expert-output buffer",
                 "parallelism": f"{world} independent replica(s)",
+                "launch": "CUDA graph replay per kernel group" if args.graph
+                          else "direct C-ABI calls (host-launched)",
                 "zero_padding": bool(args.zero_padding)}),
             "roofline": roofline,
             "cpu_baseline": cpu,

@@ -16,10 +16,9 @@ constexpr int kLayoutThreads = 256;
 constexpr int kLayoutWarps = kLayoutThreads / 32;
 constexpr int kLayoutMaxTiles = 152;
 constexpr int kMinTilePairs = 256;
-// Tokens whose destination ranks the count kernel stages at a time.
-constexpr int kRankSubTokens = 256;
 // int32 entries per shared-memory buffer when streaming the tile counts.
 constexpr int kScanChunkInts = 8192;
+
 
 struct TileGeom {
   int tile_tokens;  // tokens per tile (last tile may be short)

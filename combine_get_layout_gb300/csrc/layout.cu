@@ -67,6 +67,103 @@ __device__ __forceinline__ int read_expert(const int64_t* __restrict__ p,
   return static_cast<int>(v);
 }
 
+
+// 4 bits of m -> 4 bytes of 0/1 (bit i -> byte i).
+__device__ __forceinline__ uint32_t spread4(uint64_t m) {
+  return (static_cast<uint32_t>(m & 0xFu) * 0x204081u) & 0x01010101u;
+}
+
+// Writes one row of is_token_in_rank (R bytes, byte r = bit r of mask) with
+// the widest stores the row's alignment allows (rows start at t * R).
+__device__ __forceinline__ void write_rank_row(uint8_t* row, int R, uint64_t mask) {
+  if ((R & 15) == 0) {
+    for (int i = 0; i < R; i += 16)
+      *reinterpret_cast<uint4*>(row + i) =
+          make_uint4(spread4(mask >> i), spread4(mask >> (i + 4)),
+                     spread4(mask >> (i + 8)), spread4(mask >> (i + 12)));
+  } else if ((R & 7) == 0) {
+    for (int i = 0; i < R; i += 8)
+      *reinterpret_cast<uint2*>(row + i) =
+          make_uint2(spread4(mask >> i), spread4(mask >> (i + 4)));
+  } else if ((R & 3) == 0) {
+    for (int i = 0; i < R; i += 4) *reinterpret_cast<uint32_t*>(row + i) = spread4(mask >> i);
+  } else {
+    for (int r = 0; r < R; ++r) row[r] = static_cast<uint8_t>((mask >> r) & 1u);
+  }
+}
+
+// Pairs per unrolled round of a warp: U steps, loads issued before use.
+constexpr int kSurveyUnroll = 4;
+
+// One warp step over the selections of whole tokens: lanes [0, TPS*K) hold
+// the pairs [base, base + TPS*K) of the tile (lanes past `pe` or past the
+// step hold e = -1).  Counts experts into `hist` (leader lanes only; atomics
+// when several warps share it), flags an expert repeated within a token, and
+// writes the tokens' destination-rank rows and per-rank token counts.
+// `sr` is this warp's 32-int shared scratch.  All lanes call.
+template <bool kSharedHist>
+__device__ __forceinline__ void survey_step(int e, int lane, int base, int pe, int K,
+                                            int TPS, int Eg, int R, int32_t* hist,
+                                            int32_t* sr, uint8_t* itr_tile,
+                                            int32_t* s_rank, int& errbits) {
+  uint32_t peers = __match_any_sync(0xffffffffu, e);
+  if (e >= 0 && lane == __ffs(peers) - 1) {
+    if (kSharedHist) atomicAdd(&hist[e], __popc(peers));
+    else hist[e] += __popc(peers);
+  }
+  // the same expert twice in one token: equal (expert, token-in-step) keys
+  const int key = e >= 0 ? ((e << 5) | (lane / K)) : -1 - lane;
+  const uint32_t same = __match_any_sync(0xffffffffu, key);  // all lanes execute it
+  if (e >= 0 && __popc(same) > 1) errbits |= ERRBIT_DUP_EXPERT;
+  sr[lane] = e >= 0 ? e / Eg : -1;
+  __syncwarp();
+  if (lane < TPS && base + lane * K < pe) {
+    const int32_t* mine = sr + lane * K;
+    const int tl = base / K + lane;  // token index within the tile
+    if (R <= 64) {
+      uint64_t mask = 0;
+      for (int k = 0; k < K; ++k)
+        if (mine[k] >= 0) mask |= uint64_t(1) << mine[k];
+      write_rank_row(itr_tile + int64_t(tl) * R, R, mask);
+      for (uint64_t m = mask; m; m &= m - 1) atomicAdd(&s_rank[__ffsll(m) - 1], 1);
+    } else {
+      uint8_t* row = itr_tile + int64_t(tl) * R;
+      for (int r = 0; r < R; ++r) {
+        int in = 0;
+        for (int k = 0; k < K; ++k) in |= mine[k] == r;
+        row[r] = static_cast<uint8_t>(in);
+        if (in) atomicAdd(&s_rank[r], 1);
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// A warp's whole survey of its token-aligned span [tb, te) of a tile.
+template <bool kSharedHist>
+__device__ __forceinline__ void survey_span(const int64_t* __restrict__ src, int tb, int te,
+                                            int K, int E, int R, int lane, int32_t* hist,
+                                            int32_t* sr, uint8_t* itr_tile,
+                                            int32_t* s_rank, int& errbits) {
+  const int TPS = 32 / K, SP = TPS * K, Eg = E / R;
+  const int pb = tb * K, pe = te * K;
+  for (int b0 = pb; b0 < pe; b0 += SP * kSurveyUnroll) {
+    int ev[kSurveyUnroll];
+#pragma unroll
+    for (int u = 0; u < kSurveyUnroll; ++u) {
+      const int p = b0 + u * SP + lane;
+      ev[u] = (lane < SP && p < pe) ? read_expert(src + p, E, errbits) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kSurveyUnroll; ++u) {
+      const int base = b0 + u * SP;
+      if (base >= pe) break;
+      survey_step<kSharedHist>(ev[u], lane, base, pe, K, TPS, Eg, R, hist, sr, itr_tile,
+                               s_rank, errbits);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // 1. count
 // ---------------------------------------------------------------------------
@@ -81,8 +178,8 @@ __global__ void __launch_bounds__(kLayoutThreads)
   __shared__ int32_t s_err;
   int32_t* hist = smem_i32;            // [Epad]
   int32_t* rcnt = hist + Epad;         // [R]
-  int32_t* srank = rcnt + R;           // [kRankSubTokens * K]
-  const int tid = threadIdx.x, lane = tid & 31;
+  int32_t* wscr = rcnt + R;            // [kLayoutWarps * 32]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   if (tid == 0) s_err = 0;
   for (int e = tid; e < Epad; e += blockDim.x) hist[e] = 0;
@@ -94,49 +191,14 @@ __global__ void __launch_bounds__(kLayoutThreads)
   const int tile = blockIdx.x;
   const int t0 = tile * tile_tokens;
   const int nt = min(tile_tokens, T - t0);
-  const int P = nt * K;
   const int64_t* src = topk_idx + int64_t(t0) * K;
   int err = 0;
-
-  // Expert histogram.  Lanes holding the same expert are grouped with
-  // match.any; only the group's first lane touches shared memory, so a hot
-  // expert (skewed routing) costs one atomic per warp, not one per lane.
-  for (int base = 0; base < P; base += blockDim.x) {
-    const int p = base + tid;
-    const int e = p < P ? read_expert(src + p, E, err) : -1;
-    const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[e], __popc(peers));
-  }
-
-  // Destination ranks: a token goes once to every rank owning one of its
-  // experts (owner rank = expert / experts-per-rank); an expert may appear
-  // once per token (-1 may repeat).
-  const int Eg = E / R;
-  for (int tb = 0; tb < nt; tb += kRankSubTokens) {
-    const int ns = min(kRankSubTokens, nt - tb);
-    for (int t = tid; t < ns; t += blockDim.x) {
-      const int64_t* row = src + int64_t(tb + t) * K;
-      for (int k = 0; k < K; ++k) {
-        int ignored = 0;
-        const int e = read_expert(row + k, E, ignored);
-        srank[t * K + k] = e >= 0 ? e / Eg : -1;
-        if (e >= 0)
-          for (int k2 = 0; k2 < k; ++k2)
-            if (row[k2] == e) err |= ERRBIT_DUP_EXPERT;
-      }
-    }
-    __syncthreads();
-    uint8_t* out = is_token_in_rank + int64_t(t0 + tb) * R;
-    for (int i = tid; i < ns * R; i += blockDim.x) {
-      const int t = i / R;
-      const int r = i - t * R;
-      int in = 0;
-      for (int k = 0; k < K; ++k) in |= srank[t * K + k] == r;
-      out[i] = static_cast<uint8_t>(in);
-      if (in) atomicAdd(&rcnt[r], 1);
-    }
-    __syncthreads();
-  }
+  // Warps take token-aligned spans: expert histogram (warp-aggregated
+  // shared atomics), duplicate experts, destination ranks.
+  const int span = (nt + kLayoutWarps - 1) / kLayoutWarps;
+  const int tb = min(nt, warp * span), te = min(nt, tb + span);
+  survey_span<true>(src, tb, te, K, E, R, lane, hist, wscr + warp * 32,
+                    is_token_in_rank + int64_t(t0) * R, rcnt, err);
   if (err) atomicOr(&s_err, err);
   __syncthreads();
 
@@ -277,11 +339,19 @@ __global__ void __launch_bounds__(kLayoutThreads)
   }
   const int64_t* src = topk_idx + int64_t(t0) * K;
   int32_t* my = whist + warp * E;
-  for (int b0 = pb; b0 < pe; b0 += 32) {
-    const int p = b0 + lane;
-    const int e = p < pe ? read_expert(src + p, E, ignored) : -1;
-    const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+  for (int b0 = pb; b0 < pe; b0 += 32 * kSurveyUnroll) {
+    int ev[kSurveyUnroll];
+#pragma unroll
+    for (int u = 0; u < kSurveyUnroll; ++u) {
+      const int p = b0 + u * 32 + lane;
+      ev[u] = p < pe ? read_expert(src + p, E, ignored) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kSurveyUnroll; ++u) {
+      if (b0 + u * 32 >= pe) break;
+      const uint32_t peers = __match_any_sync(0xffffffffu, ev[u]);
+      if (ev[u] >= 0 && lane == __ffs(peers) - 1) my[ev[u]] += __popc(peers);
+    }
   }
 
   // Per expert: rows of earlier tiles (this tile's base) and of all tiles.
@@ -350,21 +420,30 @@ __global__ void __launch_bounds__(kLayoutThreads)
 
     // Pass 2: rows, in (t, k) order within each expert.
     const uint32_t lt = lanemask_lt();
-    for (int b0 = pb; b0 < pe; b0 += 32) {
-      const int p = b0 + lane;
-      const bool in = p < pe;
-      const int e = in ? read_expert(src + p, E, ignored) : -1;
-      const uint32_t peers = __match_any_sync(0xffffffffu, e);
-      int slot = -1;
-      if (e >= 0) slot = my[e] + __popc(peers & lt);
-      __syncwarp();
-      if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
-      __syncwarp();
-      if (in) {
-        slot_of[int64_t(t0) * K + p] = slot;
-        if (slot >= 0) {
-          const int tl = p / K;
-          src_info2[slot] = make_int2(t0 + tl, p - tl * K);
+    for (int b0 = pb; b0 < pe; b0 += 32 * kSurveyUnroll) {
+      int ev[kSurveyUnroll];
+#pragma unroll
+      for (int u = 0; u < kSurveyUnroll; ++u) {
+        const int p = b0 + u * 32 + lane;
+        ev[u] = p < pe ? read_expert(src + p, E, ignored) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kSurveyUnroll; ++u) {
+        if (b0 + u * 32 >= pe) break;
+        const int p = b0 + u * 32 + lane;
+        const int e = ev[u];
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        int slot = -1;
+        if (e >= 0) slot = my[e] + __popc(peers & lt);
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+        __syncwarp();
+        if (p < pe) {
+          slot_of[int64_t(t0) * K + p] = slot;
+          if (slot >= 0) {
+            const int tl = p / K;
+            src_info2[slot] = make_int2(t0 + tl, p - tl * K);
+          }
         }
       }
     }
@@ -402,15 +481,17 @@ __global__ void __launch_bounds__(kLayoutThreads)
     if (tid == 0) tokens_per_rank[r] = s_scr[34];
   }
 
-  // Alignment padding rows carry no token.
-  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+  // Alignment padding rows carry no token (one warp per expert at a time).
+  for (int e = blockIdx.x * kLayoutWarps + warp; e < E; e += gridDim.x * kLayoutWarps) {
     const int s0 = s_start[e] + s_total[e], s1 = s_start[e + 1];
-    for (int s = s0 + tid; s < s1; s += blockDim.x) src_info2[s] = make_int2(-1, -1);
+    for (int s = s0 + lane; s < s1; s += 32) src_info2[s] = make_int2(-1, -1);
   }
 }
 
+
 static int count_smem(int E, int R, int K) {
-  return (padded_experts(E) + R + kRankSubTokens * K) * 4;
+  (void)K;
+  return (padded_experts(E) + R + kLayoutWarps * 32) * 4;
 }
 
 cudaError_t prepare_layout_kernels() {
