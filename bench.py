@@ -410,7 +410,7 @@ def run_ours(args):
     recv_w = torch.empty(cap, dtype=torch.float32, device=device)
     y_d = torch.empty((T, H), dtype=torch.bfloat16, device=device)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
     def l2_flush():
         flush_w.zero_()

@@ -5,8 +5,8 @@
 // accumulation and a single final bf16 cast, so that no bf16 subtotal loses
 // a small term).
 //
-// One CTA per token.  Each thread owns 8 channels (one 16-byte vector) at a
-// time, issues the loads of all of the token's selected rows for that
+// One CTA per token (or per slice of a token's row when tokens are few).
+// Each thread owns 8 channels (one 16-byte vector) at a time, issues the loads of all of the token's selected rows for that
 // vector together (up to 8 x 16 bytes in flight per thread), then folds
 // them in ascending k with fmaf, acc starting at +0.0f, and stores one
 // 16-byte vector of bf16 rounded to nearest even.
@@ -20,12 +20,16 @@ constexpr int kCombineKBatch = 8;
 __global__ void __launch_bounds__(256)
     combine_kernel(const uint4* __restrict__ Y, const float* __restrict__ w,
                    const int32_t* __restrict__ slot_of, int H, int K,
-                   uint4* __restrict__ y) {
+                   int slices, uint4* __restrict__ y) {
   __shared__ int32_t s_slot[32];
   __shared__ float s_w[32];
-  const int t = blockIdx.x;
+  // CTA = (token, slice of the row): few tokens still fill the GPU.
+  const int t = blockIdx.x / slices;
+  const int slice = blockIdx.x - t * slices;
   const int tid = threadIdx.x;
   const int nvec = H >> 3;
+  const int per = (nvec + slices - 1) / slices;
+  const int v0 = slice * per, v1 = min(nvec, v0 + per);
   pdl_wait();
   pdl_launch_dependents();
   if (tid < K) {
@@ -34,7 +38,7 @@ __global__ void __launch_bounds__(256)
   }
   __syncthreads();
 
-  for (int v = tid; v < nvec; v += blockDim.x) {
+  for (int v = v0 + tid; v < v1; v += blockDim.x) {
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
@@ -71,13 +75,24 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// CTAs wanted in flight before rows are split across CTAs.
+constexpr int kCombineMinCtas = 2048;
+
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
   const int nvec = a.H / 8;
   const int threads = nvec >= 128 ? 128 : ((nvec + 31) / 32) * 32;
-  return launch_pdl(combine_kernel, dim3(a.T), dim3(threads), 0, stream,
+  // Split each row into slices of at least `threads` vectors when there are
+  // too few tokens to keep the GPU's memory system busy.
+  int slices = 1;
+  if (a.T < kCombineMinCtas) {
+    slices = (kCombineMinCtas + a.T - 1) / a.T;
+    const int max_slices = (nvec + threads - 1) / threads;
+    if (slices > max_slices) slices = max_slices;
+  }
+  return launch_pdl(combine_kernel, dim3(a.T * slices), dim3(threads), 0, stream,
                     static_cast<const uint4*>(a.expert_out), a.topk_weights,
-                    a.slot_of, a.H, a.K, static_cast<uint4*>(a.y));
+                    a.slot_of, a.H, a.K, slices, static_cast<uint4*>(a.y));
 }
 
 }  // namespace ep

@@ -16,7 +16,10 @@ constexpr int kLayoutThreads = 256;
 constexpr int kLayoutWarps = kLayoutThreads / 32;
 constexpr int kLayoutMaxTiles = 152;
 constexpr int kMinTilePairs = 256;
-// int32 entries per shared-memory buffer when streaming the tile counts.
+// The assign kernel loads the whole tile-count matrix with one bulk copy
+// when it has at most kScanWholeInts entries; otherwise it streams it
+// through two buffers of kScanChunkInts entries.
+constexpr int kScanWholeInts = 40960;
 constexpr int kScanChunkInts = 8192;
 
 

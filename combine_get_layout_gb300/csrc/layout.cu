@@ -252,13 +252,20 @@ struct AssignSmem {
 __host__ __device__ inline AssignSmem assign_smem(int E, int num_tiles) {
   const int Epad = padded_experts(E);
   AssignSmem s;
-  int rows = kScanChunkInts / Epad;
-  if (rows < 1) rows = 1;
-  if (num_tiles >= 1 && rows > num_tiles) rows = num_tiles;
+  int rows, nbuf;
+  if (num_tiles >= 1 && num_tiles * Epad <= kScanWholeInts) {
+    rows = num_tiles;  // the whole matrix in one bulk copy
+    nbuf = 1;
+  } else {
+    rows = kScanChunkInts / Epad;
+    if (rows < 1) rows = 1;
+    if (num_tiles >= 1 && rows > num_tiles) rows = num_tiles;
+    nbuf = 2;
+  }
   s.chunk_rows = rows;
   s.bar = 0;                                   // 2 x 8 bytes, padded
-  s.ring = 16;                                 // 2 x rows x Epad int32
-  s.whist = s.ring + 2 * rows * Epad * 4;      // kLayoutWarps x E
+  s.ring = 16;                                 // nbuf x rows x Epad int32
+  s.whist = s.ring + nbuf * rows * Epad * 4;   // kLayoutWarps x E
   s.start = s.whist + kLayoutWarps * E * 4;    // E + 1
   s.base = s.start + ((E + 1 + 3) & ~3) * 4;   // E
   s.total = s.base + Epad * 4;                 // E
