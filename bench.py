@@ -61,6 +61,14 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=12.0)
+    p.add_argument("--bias", type=int, choices=[0, 1, 2], default=0,
+                   help="combine epilogue: number of bf16 bias tensors")
+    p.add_argument("--return-weights", action="store_true",
+                   help="combine epilogue: also return the per-(t,k) gate weights")
+    p.add_argument("--fp8-scales", choices=["row", "col"], default="row",
+                   help="FP8 scale layout (col: column-major, TMA-aligned)")
+    p.add_argument("--fp8-prequant", action="store_true",
+                   help="FP8 dispatch of pre-quantised rows + scales (bit copies)")
     p.add_argument("--graph", action="store_true",
                    help="replay each kernel group from a captured CUDA graph "
                         "(removes host launch overhead; for latency-bound sizes)")
@@ -71,13 +79,17 @@ def parse_args():
 # accounting
 # ---------------------------------------------------------------------------
 
-def algorithmic_bytes(wl, n_rows: int) -> dict:
+def algorithmic_bytes(wl, n_rows: int, nbias: int = 0, return_weights: bool = False,
+                      prequant: bool = False) -> dict:
     """Bytes the method must move (each source row once, each destination row
     once, plus route metadata), per launch."""
     T, H, K, E, R = wl.num_tokens, wl.hidden, wl.num_topk, wl.num_experts, wl.num_ranks
     rowbytes = (H + 4 * (H // 128)) if wl.use_fp8_dispatch else 2 * H
-    dispatch = T * H * 2 + n_rows * rowbytes + T * K * (4 + 4) + n_rows * 4
-    combine = n_rows * H * 2 + T * H * 2 + T * K * (4 + 4)
+    src_bytes = T * rowbytes if prequant else T * H * 2
+    dispatch = src_bytes + n_rows * rowbytes + T * K * (4 + 4) + n_rows * 4
+    combine = n_rows * H * 2 + T * H * 2 + T * K * (4 + 4) + nbias * T * H * 2
+    if return_weights:
+        combine += T * K * (4 + 4)
     layout = T * K * 8 + T * K * 4 + n_rows * 8 + T * R
     return {"dispatch": dispatch, "combine": combine, "layout": layout}
 
@@ -424,13 +436,39 @@ def run_ours(args):
         st = ep.ep_get_layout(ccfg, T, p(idx_d), L.c, None, fn_stream[0])
         assert st == 0, ep.ep_status_str(st)
 
+    fp8_opts = wl.use_fp8_dispatch and (args.fp8_scales == "col" or args.fp8_prequant)
+    if fp8_opts and args.fp8_scales == "col":
+        recv_s = torch.empty((H // 128, ep.ep_scale_ld(ccfg)), dtype=torch.float32,
+                             device=device)
+    xq_d = xs_d = None
+    if wl.use_fp8_dispatch and args.fp8_prequant:  # synthetic E4M3 rows + scales
+        xq_d = torch.randint(0, 0x7E, (T, H), generator=g, device=device,
+                             dtype=torch.int32).to(torch.uint8)
+        xs_d = torch.rand((T, H // 128), generator=g, device=device)
+    epilogue = args.bias > 0 or args.return_weights
+    biases = [torch.randn((T, H), generator=g, device=device).to(torch.bfloat16)
+              for _ in range(args.bias)]
+    comb_w = (torch.empty((T, K), dtype=torch.float32, device=device)
+              if args.return_weights else None)
+
     def dispatch(xsrc):
-        st = ep.ep_dispatch(ccfg, L.c, p(xsrc), p(w_d), p(recv_x), p(recv_s), p(recv_w),
-                            fn_stream[0])
+        if fp8_opts:
+            st = ep.ep_dispatch_fp8(ccfg, L.c, None if xq_d is not None else p(xsrc),
+                                    p(xq_d), p(xs_d), p(w_d), p(recv_x), p(recv_s),
+                                    args.fp8_scales == "col", p(recv_w), fn_stream[0])
+        else:
+            st = ep.ep_dispatch(ccfg, L.c, p(xsrc), p(w_d), p(recv_x), p(recv_s), p(recv_w),
+                                fn_stream[0])
         assert st == 0, ep.ep_status_str(st)
 
     def combine(Y, out):
-        st = ep.ep_combine(ccfg, L.c, p(Y), p(w_d), p(out), fn_stream[0])
+        if epilogue:
+            b0 = p(biases[0]) if len(biases) > 0 else None
+            b1 = p(biases[1]) if len(biases) > 1 else None
+            st = ep.ep_combine_epilogue(ccfg, L.c, p(Y), p(w_d), b0, b1, p(recv_w),
+                                        p(out), p(comb_w), fn_stream[0])
+        else:
+            st = ep.ep_combine(ccfg, L.c, p(Y), p(w_d), p(out), fn_stream[0])
         assert st == 0, ep.ep_status_str(st)
 
     # layout: count + assign (assign alone when T == 0); dispatch (+ padding);
@@ -494,7 +532,8 @@ def run_ours(args):
     value, ms = job_throughput(T, ms_local, world, device)
 
     peak, peak_src = load_peaks()
-    b = algorithmic_bytes(wl, n_rows)
+    b = algorithmic_bytes(wl, n_rows, args.bias, args.return_weights,
+                          wl.use_fp8_dispatch and args.fp8_prequant)
     dis_avg, com_avg = statistics.mean(dis_ms), statistics.mean(com_ms)
     dis_gbs = b["dispatch"] / (dis_avg * 1e-3) / 1e9
     com_gbs = b["combine"] / (com_avg * 1e-3) / 1e9
@@ -590,7 +629,11 @@ def run_ours(args):
                 "parallelism": f"{world} independent replica(s)",
                 "launch": "CUDA graph replay per kernel group" if args.graph
                           else "direct C-ABI calls (host-launched)",
-                "zero_padding": bool(args.zero_padding)}),
+                "zero_padding": bool(args.zero_padding),
+                "combine_bias_tensors": args.bias,
+                "combine_returns_weights": bool(args.return_weights),
+                "fp8_scales": (args.fp8_scales if wl.use_fp8_dispatch else None),
+                "fp8_prequantised_input": bool(wl.use_fp8_dispatch and args.fp8_prequant)}),
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,

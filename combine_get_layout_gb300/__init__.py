@@ -39,6 +39,9 @@ ABI_SYMBOLS = (
     "ep_get_layout",
     "ep_dispatch",
     "ep_combine",
+    "ep_scale_ld",
+    "ep_dispatch_fp8",
+    "ep_combine_epilogue",
     "ep_check_error",
     "ep_selftest_wait_timeout",
     "ep_last_cuda_error",
@@ -95,6 +98,12 @@ def _load():
     L.ep_dispatch.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp, vp]
     L.ep_combine.restype = i32
     L.ep_combine.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp]
+    L.ep_scale_ld.restype = i64
+    L.ep_scale_ld.argtypes = [P(EpConfig)]
+    L.ep_dispatch_fp8.restype = i32
+    L.ep_dispatch_fp8.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp, vp, i32, vp, vp]
+    L.ep_combine_epilogue.restype = i32
+    L.ep_combine_epilogue.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp, vp, vp, vp]
     L.ep_check_error.restype = i32
     L.ep_check_error.argtypes = [P(EpLayout), vp]
     L.ep_selftest_wait_timeout.restype = i32
@@ -141,6 +150,24 @@ def ep_dispatch(cfg, layout, d_x, d_topk_weights, d_recv_x, d_recv_scale,
 def ep_combine(cfg, layout, d_expert_out, d_topk_weights, d_y, stream) -> int:
     return int(_lib.ep_combine(ctypes.byref(cfg), ctypes.byref(layout),
                                d_expert_out, d_topk_weights, d_y, stream))
+
+
+def ep_scale_ld(cfg: EpConfig) -> int:
+    return int(_lib.ep_scale_ld(ctypes.byref(cfg)))
+
+
+def ep_dispatch_fp8(cfg, layout, d_x, d_x_q, d_x_scale, d_topk_weights, d_recv_q,
+                    d_recv_scale, scale_col_major, d_recv_w, stream) -> int:
+    return int(_lib.ep_dispatch_fp8(ctypes.byref(cfg), ctypes.byref(layout), d_x, d_x_q,
+                                    d_x_scale, d_topk_weights, d_recv_q, d_recv_scale,
+                                    int(scale_col_major), d_recv_w, stream))
+
+
+def ep_combine_epilogue(cfg, layout, d_expert_out, d_topk_weights, d_bias0, d_bias1,
+                        d_recv_w, d_y, d_combined_w, stream) -> int:
+    return int(_lib.ep_combine_epilogue(ctypes.byref(cfg), ctypes.byref(layout),
+                                        d_expert_out, d_topk_weights, d_bias0, d_bias1,
+                                        d_recv_w, d_y, d_combined_w, stream))
 
 
 def ep_check_error(layout, stream) -> int:
@@ -310,3 +337,48 @@ def combine(cfg: Config, layout: Layout, expert_out, topk_weights=None, y=None,
 
 def check_error(layout: Layout, stream=None) -> int:
     return ep_check_error(layout.c, _stream(stream))
+
+
+def dispatch_fp8(cfg: Config, layout: Layout, x=None, x_q=None, x_scale=None,
+                 topk_weights=None, scale_col_major: bool = False, recv_q=None,
+                 recv_scale=None, recv_w=None, want_weights: bool = True, stream=None):
+    """ep_dispatch_fp8: quantise bf16 `x`, or copy pre-quantised `x_q` (uint8
+    E4M3 bits [T, H]) with `x_scale` (fp32 [T, H/128]).  Returns (recv_q,
+    recv_scale, recv_w); recv_scale is [cap, H/128], or [H/128, ld] when
+    scale_col_major."""
+    import torch
+
+    cap, H = cfg.capacity, cfg.hidden
+    dev = (x if x is not None else x_q).device
+    if recv_q is None:
+        recv_q = torch.empty((cap, H), dtype=torch.uint8, device=dev)
+    if recv_scale is None:
+        shape = (H // 128, ep_scale_ld(cfg.c())) if scale_col_major else (cap, H // 128)
+        recv_scale = torch.empty(shape, dtype=torch.float32, device=dev)
+    if want_weights and topk_weights is not None and recv_w is None:
+        recv_w = torch.empty(cap, dtype=torch.float32, device=dev)
+    st = ep_dispatch_fp8(cfg.c(), layout.c, _ptr(x), _ptr(x_q), _ptr(x_scale),
+                         _ptr(topk_weights), _ptr(recv_q), _ptr(recv_scale),
+                         scale_col_major, _ptr(recv_w), _stream(stream))
+    _check(st, "ep_dispatch_fp8")
+    return recv_q, recv_scale, recv_w
+
+
+def combine_epilogue(cfg: Config, layout: Layout, expert_out, topk_weights=None,
+                     bias0=None, bias1=None, recv_w=None, want_weights: bool = False,
+                     y=None, stream=None):
+    """ep_combine_epilogue.  Returns (y, combined_w or None)."""
+    import torch
+
+    T = layout.num_tokens
+    dev = expert_out.device
+    if y is None:
+        y = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device=dev)
+    cw = None
+    if want_weights:
+        cw = torch.empty((max(T, 1), cfg.num_topk), dtype=torch.float32, device=dev)
+    st = ep_combine_epilogue(cfg.c(), layout.c, _ptr(expert_out), _ptr(topk_weights),
+                             _ptr(bias0), _ptr(bias1), _ptr(recv_w), _ptr(y), _ptr(cw),
+                             _stream(stream))
+    _check(st, "ep_combine_epilogue")
+    return y, (None if cw is None else cw[:T])

@@ -221,6 +221,89 @@ int32_t ep_combine(const ep_config* cfg, const ep_layout* layout,
   return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
 }
 
+int64_t ep_scale_ld(const ep_config* cfg) {
+  if (!config_ok(cfg)) return -1;
+  return (capacity(cfg) + 3) / 4 * 4;
+}
+
+int32_t ep_dispatch_fp8(const ep_config* cfg, const ep_layout* layout,
+                        const void* d_x, const uint8_t* d_x_q,
+                        const float* d_x_scale, const float* d_topk_weights,
+                        uint8_t* d_recv_q, float* d_recv_scale,
+                        int32_t scale_col_major, float* d_recv_w, void* stream) {
+  if (!config_ok(cfg) || !layout_ptrs_ok(layout)) return EP_ERR_INVALID_ARG;
+  if (cfg->hidden % 128 != 0) return EP_ERR_INVALID_ARG;
+  if (scale_col_major != 0 && scale_col_major != 1) return EP_ERR_INVALID_ARG;
+  const int T = layout->num_tokens;
+  if (T < 0 || T > cfg->max_tokens) return EP_ERR_INVALID_ARG;
+  const bool prequant = d_x_q != nullptr || d_x_scale != nullptr;
+  if (prequant && (d_x != nullptr || d_x_q == nullptr || d_x_scale == nullptr))
+    return EP_ERR_INVALID_ARG;  // exactly one input form
+  if (T > 0) {
+    if (!prequant && (d_x == nullptr || !aligned16(d_x))) return EP_ERR_INVALID_ARG;
+    if (prequant && (!aligned16(d_x_q) || !aligned16(d_x_scale))) return EP_ERR_INVALID_ARG;
+  }
+  if (d_recv_q == nullptr || !aligned16(d_recv_q)) return EP_ERR_INVALID_ARG;
+  if (d_recv_scale == nullptr || !aligned16(d_recv_scale)) return EP_ERR_INVALID_ARG;
+  if (d_topk_weights != nullptr && !aligned16(d_topk_weights)) return EP_ERR_INVALID_ARG;
+  if (d_recv_w != nullptr && (!aligned16(d_recv_w) || d_topk_weights == nullptr))
+    return EP_ERR_INVALID_ARG;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
+  DispatchArgs a;
+  a.x = d_x;
+  a.topk_weights = d_topk_weights;
+  a.slot_of = layout->slot_of;
+  a.expert_start = layout->expert_start;
+  a.expert_end = layout->expert_end;
+  a.T = T;
+  a.H = cfg->hidden;
+  a.K = cfg->num_topk;
+  a.E = cfg->num_experts;
+  a.fp8 = true;
+  a.zero_padding = cfg->zero_padding != 0;
+  a.recv_x = d_recv_q;
+  a.recv_scale = d_recv_scale;
+  a.recv_w = d_recv_w;
+  a.err = layout->err;
+  a.x_q = d_x_q;
+  a.x_scale = d_x_scale;
+  a.scale_col_major = scale_col_major != 0;
+  a.scale_ld = (capacity(cfg) + 3) / 4 * 4;
+  return cuda_status(launch_dispatch(a, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t ep_combine_epilogue(const ep_config* cfg, const ep_layout* layout,
+                            const void* d_expert_out, const float* d_topk_weights,
+                            const void* d_bias0, const void* d_bias1,
+                            const float* d_recv_w, void* d_y, float* d_combined_w,
+                            void* stream) {
+  if (!config_ok(cfg) || !layout_ptrs_ok(layout)) return EP_ERR_INVALID_ARG;
+  const int T = layout->num_tokens;
+  if (T < 0 || T > cfg->max_tokens) return EP_ERR_INVALID_ARG;
+  if (T > 0) {
+    if (d_expert_out == nullptr || !aligned16(d_expert_out)) return EP_ERR_INVALID_ARG;
+    if (d_y == nullptr || !aligned16(d_y)) return EP_ERR_INVALID_ARG;
+  }
+  const void* ptrs[] = {d_topk_weights, d_bias0, d_bias1, d_recv_w, d_combined_w};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return EP_ERR_INVALID_ARG;
+  if (d_combined_w != nullptr && d_recv_w == nullptr) return EP_ERR_INVALID_ARG;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
+  CombineArgs a;
+  a.expert_out = d_expert_out;
+  a.topk_weights = d_topk_weights;
+  a.slot_of = layout->slot_of;
+  a.T = T;
+  a.H = cfg->hidden;
+  a.K = cfg->num_topk;
+  a.y = d_y;
+  a.bias0 = d_bias0;
+  a.bias1 = d_bias1;
+  a.recv_w = d_recv_w;
+  a.combined_w = d_combined_w;
+  return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
+}
+
 int32_t ep_check_error(const ep_layout* layout, void* stream) {
   if (layout == nullptr || layout->err == nullptr) return EP_ERR_INVALID_ARG;
   int32_t bits = 0;

@@ -17,10 +17,19 @@ namespace ep {
 
 constexpr int kCombineKBatch = 8;
 
+// NB: number of bf16 bias tensors added after the fold (0, 1 or 2), each in
+// fp32 and in order ("Deep Dive - DeepEP", "Combine: reverse routing plus
+// reduction": zero, one or two bias tensors in the combine epilogue).
+// combined_w (optional): the gate weight of each (t, k) read back from its
+// expert row (recv_w), 0 for an unused selection.
+template <int NB>
 __global__ void __launch_bounds__(256)
     combine_kernel(const uint4* __restrict__ Y, const float* __restrict__ w,
                    const int32_t* __restrict__ slot_of, int H, int K,
-                   int slices, uint4* __restrict__ y) {
+                   int slices, const uint4* __restrict__ b0,
+                   const uint4* __restrict__ b1,
+                   const float* __restrict__ recv_w,
+                   float* __restrict__ combined_w, uint4* __restrict__ y) {
   __shared__ int32_t s_slot[32];
   __shared__ float s_w[32];
   // CTA = (token, slice of the row): few tokens still fill the GPU.
@@ -33,8 +42,11 @@ __global__ void __launch_bounds__(256)
   pdl_wait();
   pdl_launch_dependents();
   if (tid < K) {
-    s_slot[tid] = slot_of[int64_t(t) * K + tid];
+    const int sl = slot_of[int64_t(t) * K + tid];
+    s_slot[tid] = sl;
     s_w[tid] = w != nullptr ? w[int64_t(t) * K + tid] : 1.0f;
+    if (combined_w != nullptr && slice == 0)
+      combined_w[int64_t(t) * K + tid] = sl >= 0 ? recv_w[sl] : 0.0f;
   }
   __syncthreads();
 
@@ -66,6 +78,20 @@ __global__ void __launch_bounds__(256)
         acc[7] = fmaf(wk, bf16_hi(r[j].w), acc[7]);
       }
     }
+    if (NB >= 1) {
+      const uint4 b = ld_stream_u4(b0 + int64_t(t) * nvec + v);
+      acc[0] += bf16_lo(b.x); acc[1] += bf16_hi(b.x);
+      acc[2] += bf16_lo(b.y); acc[3] += bf16_hi(b.y);
+      acc[4] += bf16_lo(b.z); acc[5] += bf16_hi(b.z);
+      acc[6] += bf16_lo(b.w); acc[7] += bf16_hi(b.w);
+    }
+    if (NB >= 2) {
+      const uint4 b = ld_stream_u4(b1 + int64_t(t) * nvec + v);
+      acc[0] += bf16_lo(b.x); acc[1] += bf16_hi(b.x);
+      acc[2] += bf16_lo(b.y); acc[3] += bf16_hi(b.y);
+      acc[4] += bf16_lo(b.z); acc[5] += bf16_hi(b.z);
+      acc[6] += bf16_lo(b.w); acc[7] += bf16_hi(b.w);
+    }
     uint4 o;
     o.x = pack_bf16x2(acc[0], acc[1]);
     o.y = pack_bf16x2(acc[2], acc[3]);
@@ -90,9 +116,21 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
     const int max_slices = (nvec + threads - 1) / threads;
     if (slices > max_slices) slices = max_slices;
   }
-  return launch_pdl(combine_kernel, dim3(a.T * slices), dim3(threads), 0, stream,
-                    static_cast<const uint4*>(a.expert_out), a.topk_weights,
-                    a.slot_of, a.H, a.K, slices, static_cast<uint4*>(a.y));
+  // Biases in the order given; a single one always goes in the first slot.
+  const uint4* b0 = static_cast<const uint4*>(a.bias0 != nullptr ? a.bias0 : a.bias1);
+  const uint4* b1 = static_cast<const uint4*>(a.bias0 != nullptr ? a.bias1 : nullptr);
+  const int nb = (b0 != nullptr) + (b1 != nullptr);
+  const dim3 grid(a.T * slices), block(threads);
+  const uint4* Y = static_cast<const uint4*>(a.expert_out);
+  uint4* y = static_cast<uint4*>(a.y);
+  if (nb == 0)
+    return launch_pdl(combine_kernel<0>, grid, block, 0, stream, Y, a.topk_weights,
+                      a.slot_of, a.H, a.K, slices, b0, b1, a.recv_w, a.combined_w, y);
+  if (nb == 1)
+    return launch_pdl(combine_kernel<1>, grid, block, 0, stream, Y, a.topk_weights,
+                      a.slot_of, a.H, a.K, slices, b0, b1, a.recv_w, a.combined_w, y);
+  return launch_pdl(combine_kernel<2>, grid, block, 0, stream, Y, a.topk_weights,
+                    a.slot_of, a.H, a.K, slices, b0, b1, a.recv_w, a.combined_w, y);
 }
 
 }  // namespace ep

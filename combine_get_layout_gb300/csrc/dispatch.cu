@@ -56,15 +56,24 @@ __global__ void __launch_bounds__(1024)
 // ---------------------------------------------------------------------------
 // FP8 E4M3 with 1x128 scales
 // ---------------------------------------------------------------------------
+// Where the scale of (row, block) lives: row-major [cap, H/128], or
+// column-major [H/128, ld] with ld = cap rounded up to 4 (the layout for TMA
+// consumers: each block's scales are one 16-byte-aligned column).
+template <bool kColMajor>
+__device__ __forceinline__ int64_t scale_index(int64_t row, int blk, int nblk, int64_t ld) {
+  return kColMajor ? int64_t(blk) * ld + row : row * nblk + blk;
+}
+
 // One CTA per token; thread u owns 16 consecutive channels (two 16-byte
 // loads), so 8 lanes cover one 128-channel block: exact amax by three
 // shuffles, scale = amax / 448, 16 E4M3 bytes written with one 16-byte store
 // per selected expert, and the block's scale by the group's first lane.
+template <bool kColMajor>
 __global__ void __launch_bounds__(1024)
     dispatch_fp8_kernel(const uint4* __restrict__ x,
                         const float* __restrict__ w,
                         const int32_t* __restrict__ slot_of, int H, int K,
-                        uint8_t* __restrict__ recv_q,
+                        int64_t scale_ld, uint8_t* __restrict__ recv_q,
                         float* __restrict__ recv_scale,
                         float* __restrict__ recv_w) {
   __shared__ int32_t s_slot[32];
@@ -122,8 +131,50 @@ __global__ void __launch_bounds__(1024)
         const int sl = s_slot[k];
         if (sl < 0) continue;
         *reinterpret_cast<uint4*>(recv_q + int64_t(sl) * H + int64_t(u) * 16) = q;
-        if (leader) recv_scale[int64_t(sl) * nblk + (u >> 3)] = scale;
+        if (leader) recv_scale[scale_index<kColMajor>(sl, u >> 3, nblk, scale_ld)] = scale;
       }
+    }
+  }
+}
+
+// Pre-quantised input ("Deep Dive - DeepEP", "Precision: FP8 on the wire,
+// BF16 for the reduction": FP8 values plus scale factors): bit copies of the
+// token's E4M3 row (16 bytes per thread) and of its scales.
+template <bool kColMajor>
+__global__ void __launch_bounds__(1024)
+    dispatch_fp8_copy_kernel(const uint4* __restrict__ x_q,
+                             const float* __restrict__ x_scale,
+                             const float* __restrict__ w,
+                             const int32_t* __restrict__ slot_of, int H, int K,
+                             int64_t scale_ld, uint8_t* __restrict__ recv_q,
+                             float* __restrict__ recv_scale,
+                             float* __restrict__ recv_w) {
+  __shared__ int32_t s_slot[32];
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int n16 = H >> 4;      // 16-byte vectors of E4M3 per row
+  const int nblk = H >> 7;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (tid < K) {
+    const int sl = slot_of[int64_t(t) * K + tid];
+    s_slot[tid] = sl;
+    if (sl >= 0 && w != nullptr && recv_w != nullptr)
+      recv_w[sl] = w[int64_t(t) * K + tid];
+  }
+  __syncthreads();
+  for (int u = tid; u < n16; u += blockDim.x) {
+    const uint4 q = ld_stream_u4(x_q + int64_t(t) * n16 + u);
+    for (int k = 0; k < K; ++k) {
+      const int sl = s_slot[k];
+      if (sl >= 0) *reinterpret_cast<uint4*>(recv_q + int64_t(sl) * H + int64_t(u) * 16) = q;
+    }
+  }
+  for (int b = tid; b < nblk; b += blockDim.x) {
+    const float sc = x_scale[int64_t(t) * nblk + b];
+    for (int k = 0; k < K; ++k) {
+      const int sl = s_slot[k];
+      if (sl >= 0) recv_scale[scale_index<kColMajor>(sl, b, nblk, scale_ld)] = sc;
     }
   }
 }
@@ -134,7 +185,7 @@ __global__ void __launch_bounds__(1024)
 __global__ void __launch_bounds__(256)
     zero_padding_kernel(const int32_t* __restrict__ expert_start,
                         const int32_t* __restrict__ expert_end, int E,
-                        int64_t row_bytes, int scale_per_row,
+                        int64_t row_bytes, int scale_per_row, int64_t scale_ld,
                         uint8_t* __restrict__ recv_x,
                         float* __restrict__ recv_scale,
                         float* __restrict__ recv_w) {
@@ -146,9 +197,14 @@ __global__ void __launch_bounds__(256)
     uint4* dst = reinterpret_cast<uint4*>(recv_x + s0 * row_bytes);
     const int64_t nv = (s1 - s0) * row_bytes / 16;
     for (int64_t i = threadIdx.x; i < nv; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
-    if (recv_scale != nullptr)
+    if (recv_scale != nullptr && scale_ld == 0)
       for (int64_t i = s0 * scale_per_row + threadIdx.x; i < s1 * scale_per_row; i += blockDim.x)
         recv_scale[i] = 0.0f;
+    if (recv_scale != nullptr && scale_ld > 0)  // column-major scales
+      for (int64_t i = threadIdx.x; i < (s1 - s0) * scale_per_row; i += blockDim.x) {
+        const int64_t c = i / (s1 - s0), r = s0 + (i - c * (s1 - s0));
+        recv_scale[c * scale_ld + r] = 0.0f;
+      }
     if (recv_w != nullptr)
       for (int64_t s = s0 + threadIdx.x; s < s1; s += blockDim.x) recv_w[s] = 0.0f;
   }
@@ -182,10 +238,18 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
       st = launch_pdl(dispatch_bf16_kernel, dim3(a.T), dim3(threads_for(nvec)), 0,
                       stream, static_cast<const uint4*>(a.x), a.topk_weights,
                       a.slot_of, nvec, a.K, static_cast<uint4*>(a.recv_x), a.recv_w);
+    } else if (a.x_q == nullptr) {
+      auto kern = a.scale_col_major ? dispatch_fp8_kernel<true> : dispatch_fp8_kernel<false>;
+      st = launch_pdl(kern, dim3(a.T), dim3(threads_for(a.H / 16)), 0, stream,
+                      static_cast<const uint4*>(a.x), a.topk_weights, a.slot_of, a.H,
+                      a.K, a.scale_ld, static_cast<uint8_t*>(a.recv_x), a.recv_scale,
+                      a.recv_w);
     } else {
-      st = launch_pdl(dispatch_fp8_kernel, dim3(a.T), dim3(threads_for(a.H / 16)), 0,
-                      stream, static_cast<const uint4*>(a.x), a.topk_weights,
-                      a.slot_of, a.H, a.K, static_cast<uint8_t*>(a.recv_x),
+      auto kern = a.scale_col_major ? dispatch_fp8_copy_kernel<true>
+                                    : dispatch_fp8_copy_kernel<false>;
+      st = launch_pdl(kern, dim3(a.T), dim3(threads_for(a.H / 16)), 0, stream,
+                      reinterpret_cast<const uint4*>(a.x_q), a.x_scale, a.topk_weights,
+                      a.slot_of, a.H, a.K, a.scale_ld, static_cast<uint8_t*>(a.recv_x),
                       a.recv_scale, a.recv_w);
     }
     if (st != cudaSuccess) return st;
@@ -195,8 +259,9 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
     int grid = a.E < 1024 ? a.E : 1024;
     st = launch_pdl(zero_padding_kernel, dim3(grid), dim3(256), 0, stream,
                     a.expert_start, a.expert_end, a.E, row_bytes,
-                    a.fp8 ? a.H / 128 : 0, static_cast<uint8_t*>(a.recv_x),
-                    a.fp8 ? a.recv_scale : nullptr, a.recv_w);
+                    a.fp8 ? a.H / 128 : 0, a.scale_col_major ? a.scale_ld : int64_t(0),
+                    static_cast<uint8_t*>(a.recv_x), a.fp8 ? a.recv_scale : nullptr,
+                    a.recv_w);
     if (st != cudaSuccess) return st;
   }
   return cudaSuccess;

@@ -71,6 +71,12 @@ struct DispatchArgs {
   float* recv_scale;
   float* recv_w;
   int32_t* err;
+  // FP8 options: pre-quantised input (E4M3 rows + fp32 scales) instead of
+  // x, and column-major scales with leading dimension scale_ld.
+  const uint8_t* x_q = nullptr;
+  const float* x_scale = nullptr;
+  bool scale_col_major = false;
+  int64_t scale_ld = 0;
 };
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
@@ -81,6 +87,11 @@ struct CombineArgs {
   const int32_t* slot_of;
   int T, H, K;
   void* y;
+  // epilogue (all optional)
+  const void* bias0 = nullptr;
+  const void* bias1 = nullptr;
+  const float* recv_w = nullptr;
+  float* combined_w = nullptr;
 };
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);

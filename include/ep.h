@@ -210,6 +210,54 @@ EP_API int32_t ep_get_layout_noalloc(const ep_config *cfg, int32_t num_tokens,
                                      ep_layout *layout,
                                      int32_t *h_expert_count, void *stream);
 
+/* Leading dimension (in fp32 entries) of column-major FP8 scales:
+ * ep_recv_capacity(cfg) rounded up to a multiple of 4, so that every
+ * block's column starts on a 16-byte boundary.  -1 if the config is
+ * invalid. */
+EP_API int64_t ep_scale_ld(const ep_config *cfg);
+
+/* FP8 dispatch with options ("Deep Dive - DeepEP", "Precision: FP8 on the
+ * wire, BF16 for the reduction": the input may arrive as FP8 values plus
+ * scale factors; a column-major scale layout serves TMA-fed consumers).
+ *
+ * Input, exactly one of:
+ *   d_x       device bf16 [T, H], quantised as in ep_dispatch (1x128 blocks,
+ *             scale = amax / 448, E4M3 round to nearest even, saturating);
+ *   d_x_q + d_x_scale  device E4M3 bytes [T, H] and fp32 scales [T, H/128]
+ *             of pre-quantised rows, copied bit for bit.
+ * d_recv_q: device [cap, H] E4M3 rows (row slot_of[t,k] gets token t).
+ * d_recv_scale: device fp32; scale_col_major = 0: [cap, H/128] row-major;
+ *   1: [H/128, ep_scale_ld(cfg)] column-major (entry (row, block) at
+ *   block * ld + row).
+ * d_topk_weights / d_recv_w: as in ep_dispatch.  cfg->zero_padding clears
+ * the alignment gap rows (payload, scales in the chosen layout, weights).
+ * H % 128 == 0 is required; cfg->use_fp8_dispatch is not consulted.
+ * Returns EP_OK or an error. */
+EP_API int32_t ep_dispatch_fp8(const ep_config *cfg, const ep_layout *layout,
+                               const void *d_x, const uint8_t *d_x_q,
+                               const float *d_x_scale,
+                               const float *d_topk_weights, uint8_t *d_recv_q,
+                               float *d_recv_scale, int32_t scale_col_major,
+                               float *d_recv_w, void *stream);
+
+/* Combine with its epilogue ("Deep Dive - DeepEP", "Combine: reverse routing
+ * plus reduction": zero, one or two bf16 bias tensors in the combine
+ * epilogue; optional return of the top-k weights).
+ *
+ * As ep_combine, then in fp32 and in this order: acc += bias0[t,i] (if
+ * d_bias0), acc += bias1[t,i] (if d_bias1), then one bf16 rounding.  Biases
+ * are device bf16 [T, H]; a NULL bias is no term.
+ * d_combined_w (device fp32 [T, K], optional; needs d_recv_w, the per-row
+ * weights dispatch wrote): combined_w[t,k] = recv_w[slot_of[t,k]], 0 for an
+ * unused selection.  With both biases and d_combined_w NULL this is exactly
+ * ep_combine.  Returns EP_OK or an error. */
+EP_API int32_t ep_combine_epilogue(const ep_config *cfg, const ep_layout *layout,
+                                   const void *d_expert_out,
+                                   const float *d_topk_weights,
+                                   const void *d_bias0, const void *d_bias1,
+                                   const float *d_recv_w, void *d_y,
+                                   float *d_combined_w, void *stream);
+
 /* Synchronises `stream` and returns the status recorded in the layout's
  * device error word (EP_OK if none): routing errors found by ep_get_layout,
  * and EP_ERR_TIMEOUT if a bounded on-chip wait of a later call gave up. */

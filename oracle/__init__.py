@@ -81,6 +81,15 @@ def _declare(L):
                                       ctypes.c_int, _p, _p, _p]
     L.oracle_combine.restype = None
     L.oracle_combine.argtypes = [_i32, _i32, _i32, _p, _p, _p, _p]
+    L.oracle_combine_epilogue.restype = None
+    L.oracle_combine_epilogue.argtypes = [_i32, _i32, _i32] + [_p] * 8
+    L.oracle_scale_ld.restype = _i64
+    L.oracle_scale_ld.argtypes = [_i64]
+    L.oracle_scales_to_col_major.restype = None
+    L.oracle_scales_to_col_major.argtypes = [_i64, _i32, _p, _i64, _p]
+    L.oracle_dispatch_fp8_prequant.restype = None
+    L.oracle_dispatch_fp8_prequant.argtypes = [_i32, _i32, _i32, _i32] + [_p] * 6 + \
+        [ctypes.c_int, _p, _p, _p]
 
 
 def _ptr(a: Optional[np.ndarray]):
@@ -241,3 +250,58 @@ def combine_tokens(expert_out, topk_weights, slot_of, tokens) -> np.ndarray:
     if rows.size == 0:
         Ysub = np.zeros((1, np.asarray(expert_out).shape[1]), np.uint16)
     return combine(Ysub, w, sub)
+
+
+def combine_epilogue(expert_out, topk_weights, slot_of, bias0=None, bias1=None,
+                     recv_w=None):
+    """Combine with the epilogue: bias terms after the fold, and the gate
+    weights gathered back per (t, k).  Returns (y, combined_w or None)."""
+    Y = _c(expert_out, np.uint16)
+    H = Y.shape[1]
+    slot_of = _c(slot_of, np.int32)
+    T, K = slot_of.shape
+    w = None if topk_weights is None else _c(topk_weights, np.float32)
+    b0 = None if bias0 is None else _c(bias0, np.uint16)
+    b1 = None if bias1 is None else _c(bias1, np.uint16)
+    rw = None if recv_w is None else _c(recv_w, np.float32)
+    y = np.zeros((T, H), np.uint16)
+    cw = None if rw is None else np.zeros((T, K), np.float32)
+    lib().oracle_combine_epilogue(T, H, K, _ptr(Y), _ptr(w), _ptr(slot_of), _ptr(b0),
+                                  _ptr(b1), _ptr(rw), _ptr(y), _ptr(cw))
+    return y, cw
+
+
+def scale_ld(cap: int) -> int:
+    return int(lib().oracle_scale_ld(cap))
+
+
+def scales_to_col_major(row_major, fill=np.nan):
+    rm = _c(row_major, np.float32)
+    cap, nb = rm.shape
+    ld = scale_ld(cap)
+    col = np.full((nb, ld), fill, np.float32)
+    lib().oracle_scales_to_col_major(cap, nb, _ptr(rm), ld, _ptr(col))
+    return col
+
+
+def dispatch_fp8_prequant(x_q, x_scale, topk_weights, lay: dict, zero_padding=False,
+                          fill=0xFF):
+    """Expanded dispatch of pre-quantised FP8 rows and their scales."""
+    xq = _c(x_q, np.uint8)
+    xs = _c(x_scale, np.float32)
+    T, H = xq.shape
+    slot_of = _c(lay["slot_of"], np.int32)
+    K = slot_of.shape[1]
+    E = lay["expert_count"].shape[0]
+    cap = lay["cap"]
+    w = None if topk_weights is None else _c(topk_weights, np.float32)
+    recv_q = np.full((cap, H), fill, np.uint8)
+    recv_scale = np.full((cap, H // 128), np.nan, np.float32)
+    recv_w = np.full(cap, np.nan, np.float32)
+    lib().oracle_dispatch_fp8_prequant(T, H, K, E, _ptr(xq), _ptr(xs), _ptr(w),
+                                       _ptr(slot_of),
+                                       _ptr(_c(lay["expert_start"], np.int32)),
+                                       _ptr(_c(lay["expert_end"], np.int32)),
+                                       int(bool(zero_padding)), _ptr(recv_q),
+                                       _ptr(recv_scale), _ptr(recv_w))
+    return recv_q, recv_scale, recv_w

@@ -310,3 +310,71 @@ void oracle_combine(int32_t T, int32_t H, int32_t K, const uint16_t *Y,
       y[(int64_t)t * H + i] = oracle_f32_to_bf16(acc);
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Combine epilogue                                                          */
+/* ------------------------------------------------------------------------ */
+
+void oracle_combine_epilogue(int32_t T, int32_t H, int32_t K, const uint16_t *Y,
+                             const float *w, const int32_t *slot_of,
+                             const uint16_t *b0, const uint16_t *b1,
+                             const float *recv_w, uint16_t *y, float *combined_w) {
+  for (int32_t t = 0; t < T; ++t)
+    for (int32_t i = 0; i < H; ++i) {
+      float acc = 0.0f;
+      for (int32_t k = 0; k < K; ++k) {
+        int32_t s = slot_of[(int64_t)t * K + k];
+        if (s < 0) continue;
+        float wk = w ? w[(int64_t)t * K + k] : 1.0f;
+        acc = fmaf(wk, oracle_bf16_to_f32(Y[(int64_t)s * H + i]), acc);
+      }
+      if (b0) acc = acc + oracle_bf16_to_f32(b0[(int64_t)t * H + i]);
+      if (b1) acc = acc + oracle_bf16_to_f32(b1[(int64_t)t * H + i]);
+      y[(int64_t)t * H + i] = oracle_f32_to_bf16(acc);
+    }
+  if (combined_w && recv_w)
+    for (int32_t t = 0; t < T; ++t)
+      for (int32_t k = 0; k < K; ++k) {
+        int32_t s = slot_of[(int64_t)t * K + k];
+        combined_w[(int64_t)t * K + k] = s >= 0 ? recv_w[s] : 0.0f;
+      }
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 scale layouts, pre-quantised input                                    */
+/* ------------------------------------------------------------------------ */
+
+int64_t oracle_scale_ld(int64_t cap) { return (cap + 3) / 4 * 4; }
+
+void oracle_scales_to_col_major(int64_t cap, int32_t nb, const float *row_major,
+                                int64_t ld, float *col_major) {
+  for (int64_t r = 0; r < cap; ++r)
+    for (int32_t c = 0; c < nb; ++c)
+      col_major[(int64_t)c * ld + r] = row_major[r * nb + c];
+}
+
+void oracle_dispatch_fp8_prequant(int32_t T, int32_t H, int32_t K, int32_t E,
+                                  const uint8_t *x_q, const float *x_scale,
+                                  const float *w, const int32_t *slot_of,
+                                  const int32_t *expert_start,
+                                  const int32_t *expert_end, int zero_padding,
+                                  uint8_t *recv_q, float *recv_scale,
+                                  float *recv_w) {
+  const int32_t nb = H / 128;
+  for (int32_t t = 0; t < T; ++t)
+    for (int32_t k = 0; k < K; ++k) {
+      int32_t s = slot_of[(int64_t)t * K + k];
+      if (s < 0) continue;
+      memcpy(recv_q + (int64_t)s * H, x_q + (int64_t)t * H, (size_t)H);
+      memcpy(recv_scale + (int64_t)s * nb, x_scale + (int64_t)t * nb,
+             (size_t)nb * sizeof(float));
+      if (w && recv_w) recv_w[s] = w[(int64_t)t * K + k];
+    }
+  if (zero_padding)
+    for (int32_t e = 0; e < E; ++e)
+      for (int32_t s = expert_end[e]; s < expert_start[e + 1]; ++s) {
+        memset(recv_q + (int64_t)s * H, 0, (size_t)H);
+        for (int32_t c = 0; c < nb; ++c) recv_scale[(int64_t)s * nb + c] = 0.0f;
+        if (recv_w) recv_w[s] = 0.0f;
+      }
+}

@@ -97,6 +97,38 @@ void oracle_dispatch_fp8(int32_t T, int32_t H, int32_t K, int32_t E,
 void oracle_combine(int32_t T, int32_t H, int32_t K, const uint16_t *Y,
                     const float *w, const int32_t *slot_of, uint16_t *y);
 
+/* ---- combine epilogue ("Deep Dive - DeepEP", "Combine: reverse routing
+ * plus reduction": zero, one or two bf16 bias tensors in the combine
+ * epilogue; optional return of top-k weights) ------------------------- */
+/* y[t,i] = bf16( (fold + b0[t,i]) + b1[t,i] ), fold as in oracle_combine, the
+ * bias terms added in fp32 after it (b0/b1 may be NULL: no term).
+ * combined_w[t,k] = recv_w[slot_of[t,k]], 0 for a masked selection (NULL:
+ * not computed). */
+void oracle_combine_epilogue(int32_t T, int32_t H, int32_t K, const uint16_t *Y,
+                             const float *w, const int32_t *slot_of,
+                             const uint16_t *b0, const uint16_t *b1,
+                             const float *recv_w, uint16_t *y, float *combined_w);
+
+/* ---- FP8 scale layouts and pre-quantised input ("Deep Dive - DeepEP",
+ * "Precision: FP8 on the wire, BF16 for the reduction": input may be FP8
+ * values plus scale factors; a column-major scale layout for TMA paths) -- */
+/* Leading dimension of the column-major scale array: cap rounded up to a
+ * multiple of 4 fp32 (16 bytes). */
+int64_t oracle_scale_ld(int64_t cap);
+/* Row-major scales [cap][nb] -> column-major [nb][ld]; entries of rows that
+ * are not copied keep their value in col. */
+void oracle_scales_to_col_major(int64_t cap, int32_t nb, const float *row_major,
+                                int64_t ld, float *col_major);
+/* Pre-quantised input: recv_q[slot] = x_q[t] and recv_scale[slot] = x_scale[t]
+ * (bit copies), recv_w as in the other dispatches. */
+void oracle_dispatch_fp8_prequant(int32_t T, int32_t H, int32_t K, int32_t E,
+                                  const uint8_t *x_q, const float *x_scale,
+                                  const float *w, const int32_t *slot_of,
+                                  const int32_t *expert_start,
+                                  const int32_t *expert_end, int zero_padding,
+                                  uint8_t *recv_q, float *recv_scale,
+                                  float *recv_w);
+
 #ifdef __cplusplus
 }
 #endif
