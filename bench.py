@@ -69,6 +69,9 @@ def parse_args():
                    help="FP8 scale layout (col: column-major, TMA-aligned)")
     p.add_argument("--fp8-prequant", action="store_true",
                    help="FP8 dispatch of pre-quantised rows + scales (bit copies)")
+    p.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
+                   help="forward: layout, dispatch, combine; backward: layout, "
+                        "combine backward (with gate gradients), dispatch backward")
     p.add_argument("--graph", action="store_true",
                    help="replay each kernel group from a captured CUDA graph "
                         "(removes host launch overhead; for latency-bound sizes)")
@@ -476,7 +479,31 @@ def run_ours(args):
     launches_per_step = (2 if T > 0 else 1) + (1 if T > 0 else 0) + \
         (1 if args.zero_padding else 0) + (1 if T > 0 else 0)
 
-    run_layout, run_dispatch, run_combine = layout, lambda: dispatch(x_d), lambda: combine(Y_d, y_d)
+    backward = args.pass_ == "backward"
+    if backward:
+        dy_d = torch.randn((T, H), generator=g, device=device).to(torch.bfloat16)
+        grad_rw = torch.randn(cap, generator=g, device=device)
+        grad_Y = torch.empty((cap, H), dtype=torch.bfloat16, device=device)
+        grad_w = torch.empty((T, K), dtype=torch.float32, device=device)
+        grad_x = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        grad_w2 = torch.empty((T, K), dtype=torch.float32, device=device)
+
+        def combine_bwd():
+            st = ep.ep_combine_backward(ccfg, L.c, p(dy_d), p(w_d), p(Y_d), p(grad_Y),
+                                        p(grad_w), fn_stream[0])
+            assert st == 0, ep.ep_status_str(st)
+
+        def dispatch_bwd():
+            st = ep.ep_dispatch_backward(ccfg, L.c, p(grad_Y), p(grad_rw), p(grad_x),
+                                         p(grad_w2), fn_stream[0])
+            assert st == 0, ep.ep_status_str(st)
+
+        stage_names = ("combine_backward", "dispatch_backward")
+        run_layout, run_dispatch, run_combine = layout, combine_bwd, dispatch_bwd
+    else:
+        stage_names = ("dispatch", "combine")
+        run_layout, run_dispatch, run_combine = (layout, lambda: dispatch(x_d),
+                                                 lambda: combine(Y_d, y_d))
     if args.graph:
         # warm up (one-time per-device set-up happens outside any capture)
         run_layout(); run_dispatch(); run_combine()
@@ -532,40 +559,45 @@ def run_ours(args):
     value, ms = job_throughput(T, ms_local, world, device)
 
     peak, peak_src = load_peaks()
-    b = algorithmic_bytes(wl, n_rows, args.bias, args.return_weights,
-                          wl.use_fp8_dispatch and args.fp8_prequant)
-    dis_avg, com_avg = statistics.mean(dis_ms), statistics.mean(com_ms)
-    dis_gbs = b["dispatch"] / (dis_avg * 1e-3) / 1e9
-    com_gbs = b["combine"] / (com_avg * 1e-3) / 1e9
-    dom = "dispatch" if dis_avg >= com_avg else "combine"
-    dom_kernel = ("dispatch_fp8_kernel" if wl.use_fp8_dispatch else "dispatch_bf16_kernel") \
-        if dom == "dispatch" else "combine_kernel"
-    achieved = dis_gbs if dom == "dispatch" else com_gbs
-    traffic = profiled_traffic(dom_kernel, wl.name)
+    if backward:
+        b = {"combine_backward": T * H * 2 + 2 * n_rows * H * 2 + T * K * (4 + 4 + 4),
+             "dispatch_backward": n_rows * H * 2 + T * H * 2 + T * K * (4 + 4 + 4)}
+        kernels = {"combine_backward": "combine_backward_kernel",
+                   "dispatch_backward": "combine_kernel"}
+    else:
+        b = algorithmic_bytes(wl, n_rows, args.bias, args.return_weights,
+                              wl.use_fp8_dispatch and args.fp8_prequant)
+        kernels = {"dispatch": "dispatch_fp8_kernel" if wl.use_fp8_dispatch
+                   else "dispatch_bf16_kernel", "combine": "combine_kernel"}
+    n1, n2 = stage_names
+    avg = {n1: statistics.mean(dis_ms), n2: statistics.mean(com_ms)}
+    med = {n1: statistics.median(dis_ms), n2: statistics.median(com_ms)}
+    gbs = {n: b[n] / (avg[n] * 1e-3) / 1e9 for n in stage_names}
+    dom = n1 if avg[n1] >= avg[n2] else n2
+    dom_kernel = kernels[dom]
+    achieved = gbs[dom]
+    traffic = profiled_traffic(dom_kernel, wl.name) if not backward else None
     roofline = {"bound": "hbm", "kernel": dom_kernel, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                 else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": b[dom]}
-    dc_ms = dis_avg + com_avg
-    breakdown = {
-        "layout_us": 1e3 * statistics.mean(lay_ms),
-        "dispatch_us": 1e3 * dis_avg, "combine_us": 1e3 * com_avg,
-        "dispatch_median_us": 1e3 * statistics.median(dis_ms),
-        "combine_median_us": 1e3 * statistics.median(com_ms),
-        "dispatch_gbs": dis_gbs, "combine_gbs": com_gbs,
-        "dispatch_pct_of_8tbs": 100 * dis_gbs / NOMINAL_HBM_GBS,
-        "combine_pct_of_8tbs": 100 * com_gbs / NOMINAL_HBM_GBS,
-        "dispatch_frac_of_measured": dis_gbs / peak, "combine_frac_of_measured": com_gbs / peak,
-        "dispatch_plus_combine_tokens_per_s": T * world / (dc_ms / 1e3),
-        "dispatch_plus_combine_gbs": (b["dispatch"] + b["combine"]) / (dc_ms * 1e-3) / 1e9,
+    dc_ms = avg[n1] + avg[n2]
+    breakdown = {"layout_us": 1e3 * statistics.mean(lay_ms)}
+    for n in stage_names:
+        breakdown.update({f"{n}_us": 1e3 * avg[n], f"{n}_median_us": 1e3 * med[n],
+                          f"{n}_gbs": gbs[n], f"{n}_pct_of_8tbs": 100 * gbs[n] / NOMINAL_HBM_GBS,
+                          f"{n}_frac_of_measured": gbs[n] / peak})
+    breakdown.update({
+        f"{n1}_plus_{n2}_tokens_per_s": T * world / (dc_ms / 1e3),
+        f"{n1}_plus_{n2}_gbs": (b[n1] + b[n2]) / (dc_ms * 1e-3) / 1e9,
         "rows_dispatched": n_rows, "capacity_rows": cap,
         "wall_s_timed_region": t1 - t0,
-    }
+    })
 
     # ---- end to end through the API, host buffers ----------------------------
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not backward:
         x_h = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
         idx_h = torch.from_numpy(inp["topk_idx"]).pin_memory()
         w_h = torch.from_numpy(inp["topk_weights"]).pin_memory()
@@ -613,7 +645,7 @@ def run_ours(args):
 
     # ---- CPU baseline (rank 0, N = 1) ----------------------------------------
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not backward:
         cpu = cpu_baseline(wl, inp, args.cpu_budget_s)
 
     if rank == 0:
@@ -624,7 +656,10 @@ def run_ours(args):
             "dtype": "bf16", "data": "synthetic (seeded router simulation, PCG64; no dataset)",
             "config": workload_config(wl, extra={
                 "l2": "flushed before every step (256 MiB write, then 256 MiB read), outside the step events",
-                "step": "layout (2 kernels) + dispatch + combine; combine reads a "
+                "step": ("layout (2 kernels) + combine backward (gate gradients on) + "
+                         "dispatch backward, seeded N(0,1) dy and expert rows")
+                        if backward else
+                        "layout (2 kernels) + dispatch + combine; combine reads a "
                         "device-resident seeded N(0,1) expert-output buffer",
                 "parallelism": f"{world} independent replica(s)",
                 "launch": "CUDA graph replay per kernel group" if args.graph

@@ -42,6 +42,8 @@ ABI_SYMBOLS = (
     "ep_scale_ld",
     "ep_dispatch_fp8",
     "ep_combine_epilogue",
+    "ep_dispatch_backward",
+    "ep_combine_backward",
     "ep_check_error",
     "ep_selftest_wait_timeout",
     "ep_last_cuda_error",
@@ -104,6 +106,10 @@ def _load():
     L.ep_dispatch_fp8.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp, vp, i32, vp, vp]
     L.ep_combine_epilogue.restype = i32
     L.ep_combine_epilogue.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp, vp, vp, vp]
+    L.ep_dispatch_backward.restype = i32
+    L.ep_dispatch_backward.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp]
+    L.ep_combine_backward.restype = i32
+    L.ep_combine_backward.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp, vp]
     L.ep_check_error.restype = i32
     L.ep_check_error.argtypes = [P(EpLayout), vp]
     L.ep_selftest_wait_timeout.restype = i32
@@ -168,6 +174,20 @@ def ep_combine_epilogue(cfg, layout, d_expert_out, d_topk_weights, d_bias0, d_bi
     return int(_lib.ep_combine_epilogue(ctypes.byref(cfg), ctypes.byref(layout),
                                         d_expert_out, d_topk_weights, d_bias0, d_bias1,
                                         d_recv_w, d_y, d_combined_w, stream))
+
+
+def ep_dispatch_backward(cfg, layout, d_grad_recv, d_grad_recv_w, d_grad_x, d_grad_w,
+                         stream) -> int:
+    return int(_lib.ep_dispatch_backward(ctypes.byref(cfg), ctypes.byref(layout),
+                                         d_grad_recv, d_grad_recv_w, d_grad_x, d_grad_w,
+                                         stream))
+
+
+def ep_combine_backward(cfg, layout, d_dy, d_topk_weights, d_expert_out,
+                        d_grad_expert_out, d_grad_w, stream) -> int:
+    return int(_lib.ep_combine_backward(ctypes.byref(cfg), ctypes.byref(layout), d_dy,
+                                        d_topk_weights, d_expert_out, d_grad_expert_out,
+                                        d_grad_w, stream))
 
 
 def ep_check_error(layout, stream) -> int:
@@ -382,3 +402,42 @@ def combine_epilogue(cfg: Config, layout: Layout, expert_out, topk_weights=None,
                              _stream(stream))
     _check(st, "ep_combine_epilogue")
     return y, (None if cw is None else cw[:T])
+
+
+def dispatch_backward(cfg: Config, layout: Layout, grad_recv, grad_recv_w=None,
+                      grad_x=None, stream=None):
+    """ep_dispatch_backward.  Returns (grad_x bf16 [T, H], grad_w or None)."""
+    import torch
+
+    T = layout.num_tokens
+    dev = grad_recv.device
+    if grad_x is None:
+        grad_x = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device=dev)
+    gw = None
+    if grad_recv_w is not None:
+        gw = torch.empty((max(T, 1), cfg.num_topk), dtype=torch.float32, device=dev)
+    st = ep_dispatch_backward(cfg.c(), layout.c, _ptr(grad_recv), _ptr(grad_recv_w),
+                              _ptr(grad_x), _ptr(gw), _stream(stream))
+    _check(st, "ep_dispatch_backward")
+    return grad_x, (None if gw is None else gw[:T])
+
+
+def combine_backward(cfg: Config, layout: Layout, dy, topk_weights=None, expert_out=None,
+                     grad_expert_out=None, want_grad_w: bool = True, stream=None):
+    """ep_combine_backward.  Returns (grad_expert_out bf16 [cap, H], grad_w or
+    None); grad_w needs the forward expert rows `expert_out`."""
+    import torch
+
+    T = layout.num_tokens
+    dev = dy.device
+    if grad_expert_out is None:
+        grad_expert_out = torch.empty((cfg.capacity, cfg.hidden), dtype=torch.bfloat16,
+                                      device=dev)
+    gw = None
+    if want_grad_w and expert_out is not None:
+        gw = torch.empty((max(T, 1), cfg.num_topk), dtype=torch.float32, device=dev)
+    st = ep_combine_backward(cfg.c(), layout.c, _ptr(dy), _ptr(topk_weights),
+                             _ptr(expert_out), _ptr(grad_expert_out), _ptr(gw),
+                             _stream(stream))
+    _check(st, "ep_combine_backward")
+    return grad_expert_out, (None if gw is None else gw[:T])

@@ -304,6 +304,66 @@ int32_t ep_combine_epilogue(const ep_config* cfg, const ep_layout* layout,
   return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
 }
 
+int32_t ep_dispatch_backward(const ep_config* cfg, const ep_layout* layout,
+                             const void* d_grad_recv, const float* d_grad_recv_w,
+                             void* d_grad_x, float* d_grad_w, void* stream) {
+  if (!config_ok(cfg) || !layout_ptrs_ok(layout)) return EP_ERR_INVALID_ARG;
+  const int T = layout->num_tokens;
+  if (T < 0 || T > cfg->max_tokens) return EP_ERR_INVALID_ARG;
+  if (T > 0) {
+    if (d_grad_recv == nullptr || !aligned16(d_grad_recv)) return EP_ERR_INVALID_ARG;
+    if (d_grad_x == nullptr || !aligned16(d_grad_x)) return EP_ERR_INVALID_ARG;
+  }
+  if ((d_grad_w == nullptr) != (d_grad_recv_w == nullptr)) return EP_ERR_INVALID_ARG;
+  if (d_grad_w != nullptr && (!aligned16(d_grad_w) || !aligned16(d_grad_recv_w)))
+    return EP_ERR_INVALID_ARG;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
+  // The transpose of the bit-copy dispatch is the unweighted row sum.
+  CombineArgs a;
+  a.expert_out = d_grad_recv;
+  a.topk_weights = nullptr;
+  a.slot_of = layout->slot_of;
+  a.T = T;
+  a.H = cfg->hidden;
+  a.K = cfg->num_topk;
+  a.y = d_grad_x;
+  a.recv_w = d_grad_recv_w;
+  a.combined_w = d_grad_w;
+  return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t ep_combine_backward(const ep_config* cfg, const ep_layout* layout,
+                            const void* d_dy, const float* d_topk_weights,
+                            const void* d_expert_out, void* d_grad_expert_out,
+                            float* d_grad_w, void* stream) {
+  if (!config_ok(cfg) || !layout_ptrs_ok(layout)) return EP_ERR_INVALID_ARG;
+  const int T = layout->num_tokens;
+  if (T < 0 || T > cfg->max_tokens) return EP_ERR_INVALID_ARG;
+  if (d_grad_expert_out == nullptr || !aligned16(d_grad_expert_out)) return EP_ERR_INVALID_ARG;
+  if (T > 0 && (d_dy == nullptr || !aligned16(d_dy))) return EP_ERR_INVALID_ARG;
+  if (d_topk_weights != nullptr && !aligned16(d_topk_weights)) return EP_ERR_INVALID_ARG;
+  if (d_grad_w != nullptr &&
+      (!aligned16(d_grad_w) || d_expert_out == nullptr || !aligned16(d_expert_out)))
+    return EP_ERR_INVALID_ARG;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CombineBackwardArgs a;
+  a.dy = d_dy;
+  a.topk_weights = d_topk_weights;
+  a.slot_of = layout->slot_of;
+  a.expert_out = d_expert_out;
+  a.T = T;
+  a.H = cfg->hidden;
+  a.K = cfg->num_topk;
+  a.grad_expert_out = d_grad_expert_out;
+  a.grad_w = d_grad_w;
+  cudaError_t e = launch_combine_backward(a, s);
+  if (e == cudaSuccess && cfg->zero_padding)
+    e = launch_zero_padding_bf16(layout->expert_start, layout->expert_end,
+                                 cfg->num_experts, cfg->hidden, d_grad_expert_out, s);
+  return cuda_status(e);
+}
+
 int32_t ep_check_error(const ep_layout* layout, void* stream) {
   if (layout == nullptr || layout->err == nullptr) return EP_ERR_INVALID_ARG;
   int32_t bits = 0;

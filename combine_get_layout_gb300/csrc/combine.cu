@@ -133,4 +133,107 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
                     a.slot_of, a.H, a.K, slices, b0, b1, a.recv_w, a.combined_w, y);
 }
 
+// ---------------------------------------------------------------------------
+// combine backward
+// ---------------------------------------------------------------------------
+// For y[t] = sum_k w[t,k] * Y[slot_of[t,k]] ("Deep Dive - DeepEP", combine
+// section, backward duality -- the transpose of the weighted row sum, plus
+// the gate gradient):
+//   grad_Y[slot, i] = bf16( w[t,k] * dy[t,i] )   (fp32 product, one rounding)
+//   grad_w[t,k]     = sum_i dy[t,i] * Y[slot, i] (fp32, fixed order: each
+//                     thread folds its vectors, then a warp tree, then the
+//                     warps in order)
+// One CTA per token; KB bounds the number of selections held in registers.
+template <int KB, bool kGradW>
+__global__ void __launch_bounds__(256)
+    combine_backward_kernel(const uint4* __restrict__ dy,
+                            const float* __restrict__ w,
+                            const int32_t* __restrict__ slot_of,
+                            const uint4* __restrict__ Y, int H, int K,
+                            uint4* __restrict__ grad_Y,
+                            float* __restrict__ grad_w) {
+  __shared__ int32_t s_slot[32];
+  __shared__ float s_w[32];
+  __shared__ float s_red[8][KB];
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nvec = H >> 3;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (tid < K) {
+    s_slot[tid] = slot_of[int64_t(t) * K + tid];
+    s_w[tid] = w != nullptr ? w[int64_t(t) * K + tid] : 1.0f;
+  }
+  __syncthreads();
+
+  float part[KB];
+#pragma unroll
+  for (int k = 0; k < KB; ++k) part[k] = 0.0f;
+  for (int v = tid; v < nvec; v += blockDim.x) {
+    const uint4 g = ld_stream_u4(dy + int64_t(t) * nvec + v);
+    const float gf[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),
+                         bf16_lo(g.z), bf16_hi(g.z), bf16_lo(g.w), bf16_hi(g.w)};
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+      if (k >= K) break;
+      const int sl = s_slot[k];
+      if (sl < 0) continue;
+      const float wk = s_w[k];
+      uint4 o;
+      o.x = pack_bf16x2(wk * gf[0], wk * gf[1]);
+      o.y = pack_bf16x2(wk * gf[2], wk * gf[3]);
+      o.z = pack_bf16x2(wk * gf[4], wk * gf[5]);
+      o.w = pack_bf16x2(wk * gf[6], wk * gf[7]);
+      grad_Y[int64_t(sl) * nvec + v] = o;
+      if (kGradW) {
+        const uint4 r = ld_stream_u4(Y + int64_t(sl) * nvec + v);
+        float p = part[k];
+        p = fmaf(gf[0], bf16_lo(r.x), p);
+        p = fmaf(gf[1], bf16_hi(r.x), p);
+        p = fmaf(gf[2], bf16_lo(r.y), p);
+        p = fmaf(gf[3], bf16_hi(r.y), p);
+        p = fmaf(gf[4], bf16_lo(r.z), p);
+        p = fmaf(gf[5], bf16_hi(r.z), p);
+        p = fmaf(gf[6], bf16_lo(r.w), p);
+        p = fmaf(gf[7], bf16_hi(r.w), p);
+        part[k] = p;
+      }
+    }
+  }
+  if (kGradW) {
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+      float p = part[k];
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+      if (lane == 0) s_red[warp][k] = p;
+    }
+    __syncthreads();
+    if (tid < K) {
+      float acc = 0.0f;
+      for (int wi = 0; wi < (int)(blockDim.x >> 5); ++wi) acc += s_red[wi][tid];
+      grad_w[int64_t(t) * K + tid] = s_slot[tid] >= 0 ? acc : 0.0f;
+    }
+  }
+}
+
+cudaError_t launch_combine_backward(const CombineBackwardArgs& a, cudaStream_t stream) {
+  if (a.T == 0) return cudaSuccess;
+  const int nvec = a.H / 8;
+  const int threads = nvec >= 256 ? 256 : ((nvec + 31) / 32) * 32;
+  const uint4* dy = static_cast<const uint4*>(a.dy);
+  const uint4* Y = static_cast<const uint4*>(a.expert_out);
+  uint4* gY = static_cast<uint4*>(a.grad_expert_out);
+  const dim3 grid(a.T), block(threads);
+  const bool gw = a.grad_w != nullptr;
+  if (a.K <= 8) {
+    auto kern = gw ? combine_backward_kernel<8, true> : combine_backward_kernel<8, false>;
+    return launch_pdl(kern, grid, block, 0, stream, dy, a.topk_weights, a.slot_of, Y,
+                      a.H, a.K, gY, a.grad_w);
+  }
+  auto kern = gw ? combine_backward_kernel<32, true> : combine_backward_kernel<32, false>;
+  return launch_pdl(kern, grid, block, 0, stream, dy, a.topk_weights, a.slot_of, Y,
+                    a.H, a.K, gY, a.grad_w);
+}
+
 }  // namespace ep

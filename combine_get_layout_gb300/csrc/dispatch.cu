@@ -230,6 +230,15 @@ cudaError_t prepare_dispatch_kernels() { return cudaSuccess; }
 
 static int threads_for(int n) { return n < 1024 ? ((n + 31) / 32) * 32 : 1024; }
 
+cudaError_t launch_zero_padding_bf16(const int32_t* expert_start, const int32_t* expert_end,
+                                     int E, int H, void* rows, cudaStream_t stream) {
+  const int grid = E < 1024 ? E : 1024;
+  return launch_pdl(zero_padding_kernel, dim3(grid), dim3(256), 0, stream, expert_start,
+                    expert_end, E, int64_t(H) * 2, 0, int64_t(0),
+                    static_cast<uint8_t*>(rows), static_cast<float*>(nullptr),
+                    static_cast<float*>(nullptr));
+}
+
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
   cudaError_t st;
   if (a.T > 0) {

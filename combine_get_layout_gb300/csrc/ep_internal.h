@@ -96,6 +96,23 @@ struct CombineArgs {
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 
+struct CombineBackwardArgs {
+  const void* dy;                 // bf16 [T, H]
+  const float* topk_weights;      // [T, K] or null (weight 1)
+  const int32_t* slot_of;
+  const void* expert_out;         // bf16 [cap, H]; needed when grad_w is set
+  int T, H, K;
+  void* grad_expert_out;          // bf16 [cap, H]
+  float* grad_w;                  // [T, K] or null
+};
+
+cudaError_t launch_combine_backward(const CombineBackwardArgs& a, cudaStream_t stream);
+
+// Zeroes the alignment gap rows of a bf16 [cap, H] buffer (rows
+// [expert_end[e], expert_start[e+1])).
+cudaError_t launch_zero_padding_bf16(const int32_t* expert_start, const int32_t* expert_end,
+                                     int E, int H, void* rows, cudaStream_t stream);
+
 // One CTA waiting (bounded) on a barrier nothing completes.
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, int32_t* err, cudaStream_t stream);
 

@@ -258,6 +258,40 @@ EP_API int32_t ep_combine_epilogue(const ep_config *cfg, const ep_layout *layout
                                    const float *d_recv_w, void *d_y,
                                    float *d_combined_w, void *stream);
 
+/* Backward of dispatch ("Deep Dive - DeepEP", combine section, backward
+ * duality: dispatch and combine are transposes -- copying rows forward
+ * becomes summing their gradients backward).
+ * d_grad_recv: device bf16 [cap, H], the gradient of the dispatched rows.
+ * d_grad_x: device bf16 [T, H]; grad_x[t,i] = bf16( sum over k ascending,
+ *   slot_of[t,k] >= 0, of grad_recv[slot_of[t,k], i] ), fp32 from +0.
+ * d_grad_recv_w / d_grad_w (both or neither; device fp32 [cap] / [T, K]):
+ *   the weights rode along as copies, so grad_w[t,k] =
+ *   grad_recv_w[slot_of[t,k]], 0 for an unused selection.
+ * Returns EP_OK or an error. */
+EP_API int32_t ep_dispatch_backward(const ep_config *cfg, const ep_layout *layout,
+                                    const void *d_grad_recv,
+                                    const float *d_grad_recv_w, void *d_grad_x,
+                                    float *d_grad_w, void *stream);
+
+/* Backward of combine (same source: the transpose of the weighted row sum,
+ * and the gate gradient the surrounding autograd needs).
+ * d_dy: device bf16 [T, H], the gradient of y.
+ * d_grad_expert_out: device bf16 [cap, H]; grad[slot_of[t,k], i] =
+ *   bf16( w[t,k] * dy[t,i] ) (fp32 product, one rounding); with
+ *   d_topk_weights NULL the weight is 1 and the rows are bit copies of dy
+ *   (a dispatch of dy).  Rows of unused selections are not written;
+ *   alignment gap rows are zeroed when cfg->zero_padding.
+ * d_grad_w (optional, device fp32 [T, K]; needs d_expert_out, the forward
+ *   expert rows): grad_w[t,k] = sum_i dy[t,i] * Y[slot_of[t,k], i] in fp32 in
+ *   a fixed order (deterministic run to run), 0 for an unused selection.
+ * Gradients of the combine biases are dy itself.  Returns EP_OK or an
+ * error. */
+EP_API int32_t ep_combine_backward(const ep_config *cfg, const ep_layout *layout,
+                                   const void *d_dy, const float *d_topk_weights,
+                                   const void *d_expert_out,
+                                   void *d_grad_expert_out, float *d_grad_w,
+                                   void *stream);
+
 /* Synchronises `stream` and returns the status recorded in the layout's
  * device error word (EP_OK if none): routing errors found by ep_get_layout,
  * and EP_ERR_TIMEOUT if a bounded on-chip wait of a later call gave up. */

@@ -83,6 +83,10 @@ def _declare(L):
     L.oracle_combine.argtypes = [_i32, _i32, _i32, _p, _p, _p, _p]
     L.oracle_combine_epilogue.restype = None
     L.oracle_combine_epilogue.argtypes = [_i32, _i32, _i32] + [_p] * 8
+    L.oracle_dispatch_backward.restype = None
+    L.oracle_dispatch_backward.argtypes = [_i32, _i32, _i32] + [_p] * 5
+    L.oracle_combine_backward.restype = None
+    L.oracle_combine_backward.argtypes = [_i32, _i32, _i32] + [_p] * 6
     L.oracle_scale_ld.restype = _i64
     L.oracle_scale_ld.argtypes = [_i64]
     L.oracle_scales_to_col_major.restype = None
@@ -305,3 +309,34 @@ def dispatch_fp8_prequant(x_q, x_scale, topk_weights, lay: dict, zero_padding=Fa
                                        int(bool(zero_padding)), _ptr(recv_q),
                                        _ptr(recv_scale), _ptr(recv_w))
     return recv_q, recv_scale, recv_w
+
+
+def dispatch_backward(grad_recv, slot_of, grad_recv_w=None):
+    """Transpose of dispatch: (grad_x [T,H] bf16 bits, grad_w [T,K] or None)."""
+    G = _c(grad_recv, np.uint16)
+    H = G.shape[1]
+    slot_of = _c(slot_of, np.int32)
+    T, K = slot_of.shape
+    gw_in = None if grad_recv_w is None else _c(grad_recv_w, np.float32)
+    gx = np.zeros((T, H), np.uint16)
+    gw = None if gw_in is None else np.zeros((T, K), np.float32)
+    lib().oracle_dispatch_backward(T, H, K, _ptr(G), _ptr(gw_in), _ptr(slot_of),
+                                   _ptr(gx), _ptr(gw))
+    return gx, gw
+
+
+def combine_backward(dy, topk_weights, slot_of, cap, expert_out=None,
+                     want_grad_w=True, fill=0xFFFF):
+    """Combine backward: (grad_Y [cap,H] bf16 bits -- unwritten rows keep
+    `fill` --, grad_w [T,K] fp32 or None)."""
+    D = _c(dy, np.uint16)
+    T, H = D.shape
+    slot_of = _c(slot_of, np.int32)
+    K = slot_of.shape[1]
+    w = None if topk_weights is None else _c(topk_weights, np.float32)
+    Y = None if expert_out is None else _c(expert_out, np.uint16)
+    gY = np.full((cap, H), fill, np.uint16)
+    gw = np.zeros((T, K), np.float32) if want_grad_w else None
+    lib().oracle_combine_backward(T, H, K, _ptr(D), _ptr(w), _ptr(slot_of), _ptr(Y),
+                                  _ptr(gY), _ptr(gw))
+    return gY, gw

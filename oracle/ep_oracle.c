@@ -378,3 +378,51 @@ void oracle_dispatch_fp8_prequant(int32_t T, int32_t H, int32_t K, int32_t E,
         if (recv_w) recv_w[s] = 0.0f;
       }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Backward                                                                  */
+/* ------------------------------------------------------------------------ */
+
+void oracle_dispatch_backward(int32_t T, int32_t H, int32_t K,
+                              const uint16_t *grad_recv, const float *grad_recv_w,
+                              const int32_t *slot_of, uint16_t *grad_x,
+                              float *grad_w) {
+  for (int32_t t = 0; t < T; ++t)
+    for (int32_t i = 0; i < H; ++i) {
+      float acc = 0.0f;
+      for (int32_t k = 0; k < K; ++k) {
+        int32_t s = slot_of[(int64_t)t * K + k];
+        if (s >= 0) acc = acc + oracle_bf16_to_f32(grad_recv[(int64_t)s * H + i]);
+      }
+      grad_x[(int64_t)t * H + i] = oracle_f32_to_bf16(acc);
+    }
+  if (grad_w && grad_recv_w)
+    for (int32_t t = 0; t < T; ++t)
+      for (int32_t k = 0; k < K; ++k) {
+        int32_t s = slot_of[(int64_t)t * K + k];
+        grad_w[(int64_t)t * K + k] = s >= 0 ? grad_recv_w[s] : 0.0f;
+      }
+}
+
+void oracle_combine_backward(int32_t T, int32_t H, int32_t K, const uint16_t *dy,
+                             const float *w, const int32_t *slot_of,
+                             const uint16_t *Y, uint16_t *grad_Y, float *grad_w) {
+  for (int32_t t = 0; t < T; ++t)
+    for (int32_t k = 0; k < K; ++k) {
+      int32_t s = slot_of[(int64_t)t * K + k];
+      if (s < 0) {
+        if (grad_w) grad_w[(int64_t)t * K + k] = 0.0f;
+        continue;
+      }
+      float wk = w ? w[(int64_t)t * K + k] : 1.0f;
+      double dot = 0.0;
+      for (int32_t i = 0; i < H; ++i) {
+        float g = oracle_bf16_to_f32(dy[(int64_t)t * H + i]);
+        float prod = wk * g;
+        grad_Y[(int64_t)s * H + i] = oracle_f32_to_bf16(prod);
+        if (grad_w && Y)
+          dot += (double)g * (double)oracle_bf16_to_f32(Y[(int64_t)s * H + i]);
+      }
+      if (grad_w) grad_w[(int64_t)t * K + k] = Y ? (float)dot : 0.0f;
+    }
+}

@@ -129,6 +129,27 @@ void oracle_dispatch_fp8_prequant(int32_t T, int32_t H, int32_t K, int32_t E,
                                   uint8_t *recv_q, float *recv_scale,
                                   float *recv_w);
 
+/* ---- backward ("Deep Dive - DeepEP", combine section, backward duality:
+ * for the unweighted route operators dispatch and combine are transposes --
+ * copying rows forward becomes summing their gradients backward -- and the
+ * gate multiplication needs its own gradient) -------------------------- */
+/* Dispatch backward: grad_x[t,i] = bf16( sum over k ascending, slot_of >= 0,
+ * of grad_recv[slot, i] ), fp32 from +0.  grad_w[t,k] = grad_recv_w[slot],
+ * 0 for a masked selection (both gradient-of-weight pointers may be NULL). */
+void oracle_dispatch_backward(int32_t T, int32_t H, int32_t K,
+                              const uint16_t *grad_recv, const float *grad_recv_w,
+                              const int32_t *slot_of, uint16_t *grad_x,
+                              float *grad_w);
+/* Combine backward for y[t] = sum_k w[t,k] * Y[slot_of[t,k]] (+ biases):
+ * grad_Y[slot, i] = bf16( w[t,k] * dy[t,i] ) (fp32 product, then one bf16
+ * rounding; w == NULL: weight 1, a bit copy of dy); rows of masked or
+ * padding slots are not written.  grad_w[t,k] = sum_i dy[t,i] * Y[slot, i]
+ * evaluated in double and rounded once to fp32, 0 for a masked selection
+ * (grad_w and Y may be NULL). */
+void oracle_combine_backward(int32_t T, int32_t H, int32_t K, const uint16_t *dy,
+                             const float *w, const int32_t *slot_of,
+                             const uint16_t *Y, uint16_t *grad_Y, float *grad_w);
+
 #ifdef __cplusplus
 }
 #endif
