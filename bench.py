@@ -69,9 +69,12 @@ def parse_args():
                    help="FP8 scale layout (col: column-major, TMA-aligned)")
     p.add_argument("--fp8-prequant", action="store_true",
                    help="FP8 dispatch of pre-quantised rows + scales (bit copies)")
-    p.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
+    p.add_argument("--pass", dest="pass_", choices=["forward", "backward", "ranks"],
+                   default="forward",
                    help="forward: layout, dispatch, combine; backward: layout, "
-                        "combine backward (with gate gradients), dispatch backward")
+                        "combine backward (with gate gradients), dispatch backward; "
+                        "ranks: layout, dispatch to ranks, expand, reduce to ranks, "
+                        "combine over ranks (the non-expanded path)")
     p.add_argument("--graph", action="store_true",
                    help="replay each kernel group from a captured CUDA graph "
                         "(removes host launch overhead; for latency-bound sizes)")
@@ -417,7 +420,7 @@ def run_ours(args):
     g = torch.Generator(device=device)
     g.manual_seed(1234 + rank)
     Y_d = torch.randn((cap, H), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
-    L = ep.Layout(cfg, device=device)
+    L = ep.Layout(cfg, device=device, with_ranks=args.pass_ == "ranks")
     rx_dtype = torch.uint8 if wl.use_fp8_dispatch else torch.bfloat16
     recv_x = torch.empty((cap, H), dtype=rx_dtype, device=device)
     recv_s = (torch.empty((cap, H // 128), dtype=torch.float32, device=device)
@@ -474,12 +477,13 @@ def run_ours(args):
             st = ep.ep_combine(ccfg, L.c, p(Y), p(w_d), p(out), fn_stream[0])
         assert st == 0, ep.ep_status_str(st)
 
-    # layout: count + assign (assign alone when T == 0); dispatch (+ padding);
-    # combine
-    launches_per_step = (2 if T > 0 else 1) + (1 if T > 0 else 0) + \
-        (1 if args.zero_padding else 0) + (1 if T > 0 else 0)
-
+    # Stages of one step: (name, callable, kernels launched).  The layout is
+    # count + assign (assign alone when T == 0).
+    lay_launches = 2 if T > 0 else 1
+    one = 1 if T > 0 else 0
+    zp_extra = 1 if args.zero_padding else 0
     backward = args.pass_ == "backward"
+    ranks_pass = args.pass_ == "ranks"
     if backward:
         dy_d = torch.randn((T, H), generator=g, device=device).to(torch.bfloat16)
         grad_rw = torch.randn(cap, generator=g, device=device)
@@ -498,30 +502,63 @@ def run_ours(args):
                                          p(grad_w2), fn_stream[0])
             assert st == 0, ep.ep_status_str(st)
 
-        stage_names = ("combine_backward", "dispatch_backward")
-        run_layout, run_dispatch, run_combine = layout, combine_bwd, dispatch_bwd
+        stages = [("layout", layout, lay_launches),
+                  ("combine_backward", combine_bwd, one + zp_extra),
+                  ("dispatch_backward", dispatch_bwd, one)]
+    elif ranks_pass:
+        nrows = ep.ep_rank_rows_capacity(ccfg)
+        rank_x = torch.empty((nrows, H), dtype=torch.bfloat16, device=device)
+        rank_idx = torch.empty((nrows, K), dtype=torch.int32, device=device)
+        rank_w = torch.empty((nrows, K), dtype=torch.float32, device=device)
+        rank_y = torch.empty((nrows, H), dtype=torch.bfloat16, device=device)
+
+        def dispatch_ranks():
+            st = ep.ep_dispatch_ranks(ccfg, L.c, p(x_d), p(idx_d), p(w_d), p(rank_x),
+                                      p(rank_idx), p(rank_w), fn_stream[0])
+            assert st == 0, ep.ep_status_str(st)
+
+        def expand():
+            st = ep.ep_expand(ccfg, L.c, p(idx_d), p(rank_x), p(rank_w), p(recv_x),
+                              p(recv_w), fn_stream[0])
+            assert st == 0, ep.ep_status_str(st)
+
+        def reduce_ranks():
+            st = ep.ep_reduce_ranks(ccfg, L.c, p(idx_d), p(Y_d), p(w_d), p(rank_y),
+                                    fn_stream[0])
+            assert st == 0, ep.ep_status_str(st)
+
+        def combine_ranks():
+            st = ep.ep_combine_ranks(ccfg, L.c, p(rank_y), p(y_d), fn_stream[0])
+            assert st == 0, ep.ep_status_str(st)
+
+        stages = [("layout", layout, lay_launches),
+                  ("dispatch_ranks", dispatch_ranks, one),
+                  ("expand", expand, one + zp_extra),
+                  ("reduce_ranks", reduce_ranks, one),
+                  ("combine_ranks", combine_ranks, one)]
     else:
-        stage_names = ("dispatch", "combine")
-        run_layout, run_dispatch, run_combine = (layout, lambda: dispatch(x_d),
-                                                 lambda: combine(Y_d, y_d))
+        stages = [("layout", layout, lay_launches),
+                  ("dispatch", lambda: dispatch(x_d), one + zp_extra),
+                  ("combine", lambda: combine(Y_d, y_d), one)]
+    launches_per_step = sum(n for _, _, n in stages)
+    runners = [fn for _, fn, _ in stages]
     if args.graph:
         # warm up (one-time per-device set-up happens outside any capture)
-        run_layout(); run_dispatch(); run_combine()
+        for fn in runners:
+            fn()
         torch.cuda.synchronize()
         graphs = []
-        for fn in (run_layout, run_dispatch, run_combine):
+        for fn in runners:
             g_ = torch.cuda.CUDAGraph()
             cap_stream = torch.cuda.Stream(device)
             cap_stream.wait_stream(stream)
             with torch.cuda.graph(g_, stream=cap_stream):
-                st_ptr = ctypes.c_void_p(cap_stream.cuda_stream)
-                fn_stream[0] = st_ptr
+                fn_stream[0] = ctypes.c_void_p(cap_stream.cuda_stream)
                 fn()
                 fn_stream[0] = sptr
             graphs.append(g_)
         torch.cuda.synchronize()
-        run_layout, run_dispatch, run_combine = (graphs[0].replay, graphs[1].replay,
-                                                 graphs[2].replay)
+        runners = [g_.replay for g_ in graphs]
 
     # ---- device-resident timing ---------------------------------------------
     dev_id = str(local)
@@ -532,72 +569,84 @@ def run_ours(args):
     sampler = ClockSampler(dev_id)
     for _ in range(args.warmup):
         l2_flush()
-        run_layout(); run_dispatch(); run_combine()
+        for fn in runners:
+            fn()
     torch.cuda.synchronize()
     assert ep.ep_check_error(L.c, sptr) == 0
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    ns = len(runners)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)]
+          for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(args.steps):
         l2_flush()
         e = ev[i]
-        e[0].record(stream); run_layout()
-        e[1].record(stream); run_dispatch()
-        e[2].record(stream); run_combine()
-        e[3].record(stream)
+        for j, fn in enumerate(runners):
+            e[j].record(stream)
+            fn()
+        e[ns].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     t1 = time.perf_counter()
     sampler.stop()
     clocks = sampler.summary(t0, t1)
-    lay_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    dis_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    com_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    stage_ms = {name: [e[j].elapsed_time(e[j + 1]) for e in ev]
+                for j, (name, _, _) in enumerate(stages)}
+    step_ms = [e[0].elapsed_time(e[ns]) for e in ev]
     ms_local = statistics.mean(step_ms)
     value, ms = job_throughput(T, ms_local, world, device)
 
     peak, peak_src = load_peaks()
+    n_rank_rows = int(L.tokens_per_rank.sum()) if ranks_pass else 0
     if backward:
         b = {"combine_backward": T * H * 2 + 2 * n_rows * H * 2 + T * K * (4 + 4 + 4),
              "dispatch_backward": n_rows * H * 2 + T * H * 2 + T * K * (4 + 4 + 4)}
         kernels = {"combine_backward": "combine_backward_kernel",
                    "dispatch_backward": "combine_kernel"}
+    elif ranks_pass:
+        b = {"dispatch_ranks": T * H * 2 + n_rank_rows * (H * 2 + K * 8) + T * K * 12,
+             "expand": n_rank_rows * H * 2 + n_rows * (H * 2 + 4) + T * K * 16,
+             "reduce_ranks": n_rows * H * 2 + n_rank_rows * H * 2 + T * K * 16,
+             "combine_ranks": n_rank_rows * H * 2 + T * H * 2 + T * wl.num_ranks * 4}
+        kernels = {"dispatch_ranks": "dispatch_ranks_kernel", "expand": "expand_kernel",
+                   "reduce_ranks": "reduce_ranks_kernel", "combine_ranks": "combine_kernel"}
     else:
         b = algorithmic_bytes(wl, n_rows, args.bias, args.return_weights,
                               wl.use_fp8_dispatch and args.fp8_prequant)
         kernels = {"dispatch": "dispatch_fp8_kernel" if wl.use_fp8_dispatch
                    else "dispatch_bf16_kernel", "combine": "combine_kernel"}
-    n1, n2 = stage_names
-    avg = {n1: statistics.mean(dis_ms), n2: statistics.mean(com_ms)}
-    med = {n1: statistics.median(dis_ms), n2: statistics.median(com_ms)}
-    gbs = {n: b[n] / (avg[n] * 1e-3) / 1e9 for n in stage_names}
-    dom = n1 if avg[n1] >= avg[n2] else n2
+    streaming = [name for name, _, _ in stages if name != "layout"]
+    avg = {n: statistics.mean(stage_ms[n]) for n in streaming}
+    med = {n: statistics.median(stage_ms[n]) for n in streaming}
+    gbs = {n: b[n] / (avg[n] * 1e-3) / 1e9 for n in streaming}
+    dom = max(streaming, key=lambda n: avg[n])
     dom_kernel = kernels[dom]
     achieved = gbs[dom]
-    traffic = profiled_traffic(dom_kernel, wl.name) if not backward else None
+    traffic = profiled_traffic(dom_kernel, wl.name) if args.pass_ == "forward" else None
     roofline = {"bound": "hbm", "kernel": dom_kernel, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                 else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": b[dom]}
-    dc_ms = avg[n1] + avg[n2]
-    breakdown = {"layout_us": 1e3 * statistics.mean(lay_ms)}
-    for n in stage_names:
+    stream_ms = sum(avg.values())
+    breakdown = {"layout_us": 1e3 * statistics.mean(stage_ms["layout"])}
+    for n in streaming:
         breakdown.update({f"{n}_us": 1e3 * avg[n], f"{n}_median_us": 1e3 * med[n],
                           f"{n}_gbs": gbs[n], f"{n}_pct_of_8tbs": 100 * gbs[n] / NOMINAL_HBM_GBS,
                           f"{n}_frac_of_measured": gbs[n] / peak})
     breakdown.update({
-        f"{n1}_plus_{n2}_tokens_per_s": T * world / (dc_ms / 1e3),
-        f"{n1}_plus_{n2}_gbs": (b[n1] + b[n2]) / (dc_ms * 1e-3) / 1e9,
+        "streaming_stages_tokens_per_s": T * world / (stream_ms / 1e3),
+        "streaming_stages_gbs": sum(b[n] for n in streaming) / (stream_ms * 1e-3) / 1e9,
         "rows_dispatched": n_rows, "capacity_rows": cap,
         "wall_s_timed_region": t1 - t0,
     })
+    if ranks_pass:
+        breakdown["rank_rows"] = n_rank_rows
 
     # ---- end to end through the API, host buffers ----------------------------
     e2e = None
-    if not args.no_e2e and not backward:
+    if not args.no_e2e and args.pass_ == "forward":
         x_h = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
         idx_h = torch.from_numpy(inp["topk_idx"]).pin_memory()
         w_h = torch.from_numpy(inp["topk_weights"]).pin_memory()
@@ -645,7 +694,7 @@ def run_ours(args):
 
     # ---- CPU baseline (rank 0, N = 1) ----------------------------------------
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not backward:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.pass_ == "forward":
         cpu = cpu_baseline(wl, inp, args.cpu_budget_s)
 
     if rank == 0:
@@ -656,11 +705,9 @@ def run_ours(args):
             "dtype": "bf16", "data": "synthetic (seeded router simulation, PCG64; no dataset)",
             "config": workload_config(wl, extra={
                 "l2": "flushed before every step (256 MiB write, then 256 MiB read), outside the step events",
-                "step": ("layout (2 kernels) + combine backward (gate gradients on) + "
-                         "dispatch backward, seeded N(0,1) dy and expert rows")
-                        if backward else
-                        "layout (2 kernels) + dispatch + combine; combine reads a "
-                        "device-resident seeded N(0,1) expert-output buffer",
+                "step": " + ".join(name for name, _, _ in stages) +
+                        ("; seeded N(0,1) dy and expert rows" if backward else
+                         "; combine reads a device-resident seeded N(0,1) expert-output buffer"),
                 "parallelism": f"{world} independent replica(s)",
                 "launch": "CUDA graph replay per kernel group" if args.graph
                           else "direct C-ABI calls (host-launched)",

@@ -44,6 +44,11 @@ ABI_SYMBOLS = (
     "ep_combine_epilogue",
     "ep_dispatch_backward",
     "ep_combine_backward",
+    "ep_rank_rows_capacity",
+    "ep_dispatch_ranks",
+    "ep_expand",
+    "ep_reduce_ranks",
+    "ep_combine_ranks",
     "ep_check_error",
     "ep_selftest_wait_timeout",
     "ep_last_cuda_error",
@@ -77,6 +82,9 @@ class EpLayout(ctypes.Structure):
         ("src_info", ctypes.c_void_p),
         ("err", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p),
+        ("rank_row_start", ctypes.c_void_p),
+        ("rank_slot_of", ctypes.c_void_p),
+        ("rank_src", ctypes.c_void_p),
         ("num_tokens", ctypes.c_int32),
         ("reserved", ctypes.c_int32),
     ]
@@ -110,6 +118,16 @@ def _load():
     L.ep_dispatch_backward.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp]
     L.ep_combine_backward.restype = i32
     L.ep_combine_backward.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp, vp]
+    L.ep_rank_rows_capacity.restype = i64
+    L.ep_rank_rows_capacity.argtypes = [P(EpConfig)]
+    L.ep_dispatch_ranks.restype = i32
+    L.ep_dispatch_ranks.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp, vp, vp]
+    L.ep_expand.restype = i32
+    L.ep_expand.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp, vp]
+    L.ep_reduce_ranks.restype = i32
+    L.ep_reduce_ranks.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp]
+    L.ep_combine_ranks.restype = i32
+    L.ep_combine_ranks.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp]
     L.ep_check_error.restype = i32
     L.ep_check_error.argtypes = [P(EpLayout), vp]
     L.ep_selftest_wait_timeout.restype = i32
@@ -188,6 +206,34 @@ def ep_combine_backward(cfg, layout, d_dy, d_topk_weights, d_expert_out,
     return int(_lib.ep_combine_backward(ctypes.byref(cfg), ctypes.byref(layout), d_dy,
                                         d_topk_weights, d_expert_out, d_grad_expert_out,
                                         d_grad_w, stream))
+
+
+def ep_rank_rows_capacity(cfg: EpConfig) -> int:
+    return int(_lib.ep_rank_rows_capacity(ctypes.byref(cfg)))
+
+
+def ep_dispatch_ranks(cfg, layout, d_x, d_topk_idx, d_topk_weights, d_rank_x,
+                      d_rank_topk_idx, d_rank_topk_w, stream) -> int:
+    return int(_lib.ep_dispatch_ranks(ctypes.byref(cfg), ctypes.byref(layout), d_x,
+                                      d_topk_idx, d_topk_weights, d_rank_x,
+                                      d_rank_topk_idx, d_rank_topk_w, stream))
+
+
+def ep_expand(cfg, layout, d_topk_idx, d_rank_x, d_rank_topk_w, d_recv_x, d_recv_w,
+              stream) -> int:
+    return int(_lib.ep_expand(ctypes.byref(cfg), ctypes.byref(layout), d_topk_idx,
+                              d_rank_x, d_rank_topk_w, d_recv_x, d_recv_w, stream))
+
+
+def ep_reduce_ranks(cfg, layout, d_topk_idx, d_expert_out, d_topk_weights, d_rank_y,
+                    stream) -> int:
+    return int(_lib.ep_reduce_ranks(ctypes.byref(cfg), ctypes.byref(layout), d_topk_idx,
+                                    d_expert_out, d_topk_weights, d_rank_y, stream))
+
+
+def ep_combine_ranks(cfg, layout, d_rank_y, d_y, stream) -> int:
+    return int(_lib.ep_combine_ranks(ctypes.byref(cfg), ctypes.byref(layout), d_rank_y,
+                                     d_y, stream))
 
 
 def ep_check_error(layout, stream) -> int:
@@ -272,7 +318,7 @@ def _stream(stream=None):
 class Layout:
     """Device buffers of one layout handle, allocated with torch."""
 
-    def __init__(self, cfg: Config, device="cuda"):
+    def __init__(self, cfg: Config, device="cuda", with_ranks: bool = False):
         import torch
 
         self.cfg = cfg
@@ -290,11 +336,17 @@ class Layout:
         self.src_info = torch.full((cap, 2), -1, **i32)
         self.err = torch.zeros(4, **i32)
         self.workspace = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)
+        self.rank_row_start = self.rank_slot_of = self.rank_src = None
+        if with_ranks:
+            self.rank_row_start = torch.zeros(R + 1, **i32)
+            self.rank_slot_of = torch.full((max(T, 1), R), -1, **i32)
+            self.rank_src = torch.full((max(T * min(K, R), 1),), -1, **i32)
         self.c = EpLayout(
             _ptr(self.expert_count), _ptr(self.expert_start), _ptr(self.expert_end),
             _ptr(self.rank_start), _ptr(self.tokens_per_rank),
             _ptr(self.is_token_in_rank), _ptr(self.slot_of), _ptr(self.src_info),
-            _ptr(self.err), _ptr(self.workspace), 0, 0)
+            _ptr(self.err), _ptr(self.workspace), _ptr(self.rank_row_start),
+            _ptr(self.rank_slot_of), _ptr(self.rank_src), 0, 0)
 
     @property
     def num_tokens(self) -> int:
@@ -302,12 +354,12 @@ class Layout:
 
 
 def get_layout(cfg: Config, topk_idx, layout: Optional[Layout] = None,
-               sync: bool = False, stream=None) -> Layout:
+               sync: bool = False, stream=None, with_ranks: bool = False) -> Layout:
     """ep_get_layout on an int64 CUDA tensor [T, K]."""
     import numpy as np
 
     if layout is None:
-        layout = Layout(cfg, device=topk_idx.device)
+        layout = Layout(cfg, device=topk_idx.device, with_ranks=with_ranks)
     T = int(topk_idx.shape[0])
     h = None
     if sync:
@@ -441,3 +493,67 @@ def combine_backward(cfg: Config, layout: Layout, dy, topk_weights=None, expert_
                              _stream(stream))
     _check(st, "ep_combine_backward")
     return grad_expert_out, (None if gw is None else gw[:T])
+
+
+# ---- non-expanded (destination-major) stage ------------------------------------
+
+def dispatch_ranks(cfg: Config, layout: Layout, x, topk_idx, topk_weights=None,
+                   stream=None):
+    """ep_dispatch_ranks.  Returns (rank_x bf16 [rows_cap, H], rank_topk_idx
+    int32 [rows_cap, K], rank_topk_w fp32 [rows_cap, K] or None)."""
+    import torch
+
+    n = ep_rank_rows_capacity(cfg.c())
+    dev = x.device
+    rank_x = torch.empty((max(n, 1), cfg.hidden), dtype=torch.bfloat16, device=dev)
+    ridx = torch.empty((max(n, 1), cfg.num_topk), dtype=torch.int32, device=dev)
+    rw = None
+    if topk_weights is not None:
+        rw = torch.empty((max(n, 1), cfg.num_topk), dtype=torch.float32, device=dev)
+    st = ep_dispatch_ranks(cfg.c(), layout.c, _ptr(x), _ptr(topk_idx), _ptr(topk_weights),
+                           _ptr(rank_x), _ptr(ridx), _ptr(rw), _stream(stream))
+    _check(st, "ep_dispatch_ranks")
+    return rank_x, ridx, rw
+
+
+def expand(cfg: Config, layout: Layout, topk_idx, rank_x, rank_topk_w=None,
+           recv_x=None, stream=None):
+    """ep_expand.  Returns (recv_x bf16 [cap, H], recv_w or None)."""
+    import torch
+
+    dev = rank_x.device
+    if recv_x is None:
+        recv_x = torch.empty((cfg.capacity, cfg.hidden), dtype=torch.bfloat16, device=dev)
+    rw = None
+    if rank_topk_w is not None:
+        rw = torch.empty(cfg.capacity, dtype=torch.float32, device=dev)
+    st = ep_expand(cfg.c(), layout.c, _ptr(topk_idx), _ptr(rank_x), _ptr(rank_topk_w),
+                   _ptr(recv_x), _ptr(rw), _stream(stream))
+    _check(st, "ep_expand")
+    return recv_x, rw
+
+
+def reduce_ranks(cfg: Config, layout: Layout, topk_idx, expert_out, topk_weights=None,
+                 stream=None):
+    """ep_reduce_ranks.  Returns rank_y bf16 [rows_cap, H]."""
+    import torch
+
+    n = ep_rank_rows_capacity(cfg.c())
+    rank_y = torch.empty((max(n, 1), cfg.hidden), dtype=torch.bfloat16,
+                         device=expert_out.device)
+    st = ep_reduce_ranks(cfg.c(), layout.c, _ptr(topk_idx), _ptr(expert_out),
+                         _ptr(topk_weights), _ptr(rank_y), _stream(stream))
+    _check(st, "ep_reduce_ranks")
+    return rank_y
+
+
+def combine_ranks(cfg: Config, layout: Layout, rank_y, y=None, stream=None):
+    """ep_combine_ranks.  Returns y bf16 [T, H]."""
+    import torch
+
+    if y is None:
+        y = torch.empty((layout.num_tokens, cfg.hidden), dtype=torch.bfloat16,
+                        device=rank_y.device)
+    st = ep_combine_ranks(cfg.c(), layout.c, _ptr(rank_y), _ptr(y), _stream(stream))
+    _check(st, "ep_combine_ranks")
+    return y

@@ -101,7 +101,20 @@ static bool layout_ptrs_ok(const ep_layout* L) {
                       L->slot_of, L->src_info, L->err, L->workspace};
   for (const void* p : ps)
     if (p == nullptr || !aligned16(p)) return false;
+  // optional rank rows: all three or none
+  const void* rs[] = {L->rank_row_start, L->rank_slot_of, L->rank_src};
+  const int set = (rs[0] != nullptr) + (rs[1] != nullptr) + (rs[2] != nullptr);
+  if (set != 0 && set != 3) return false;
+  for (const void* p : rs)
+    if (p != nullptr && !aligned16(p)) return false;
   return true;
+}
+
+static bool has_rank_rows(const ep_layout* L) { return L->rank_slot_of != nullptr; }
+
+static int64_t rank_rows_capacity(const ep_config* c) {
+  const int per = c->num_topk < c->num_ranks ? c->num_topk : c->num_ranks;
+  return int64_t(c->max_tokens) * per;
 }
 
 }  // namespace ep
@@ -147,6 +160,9 @@ int32_t ep_get_layout(const ep_config* cfg, int32_t num_tokens,
   a.src_info = layout->src_info;
   a.err = layout->err;
   a.is_token_in_rank = layout->is_token_in_rank;
+  a.rank_row_start = layout->rank_row_start;
+  a.rank_slot_of = layout->rank_slot_of;
+  a.rank_src = layout->rank_src;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = note_cuda(launch_layout(a, s));
   if (e != cudaSuccess) return EP_ERR_CUDA;
@@ -362,6 +378,115 @@ int32_t ep_combine_backward(const ep_config* cfg, const ep_layout* layout,
     e = launch_zero_padding_bf16(layout->expert_start, layout->expert_end,
                                  cfg->num_experts, cfg->hidden, d_grad_expert_out, s);
   return cuda_status(e);
+}
+
+int64_t ep_rank_rows_capacity(const ep_config* cfg) {
+  return config_ok(cfg) ? rank_rows_capacity(cfg) : -1;
+}
+
+// Common checks of the non-expanded entry points.
+static int32_t rank_call_ok(const ep_config* cfg, const ep_layout* layout,
+                            const void* const* required, int n_required,
+                            const void* const* optional, int n_optional) {
+  if (!config_ok(cfg) || !layout_ptrs_ok(layout) || !has_rank_rows(layout))
+    return EP_ERR_INVALID_ARG;
+  const int T = layout->num_tokens;
+  if (T < 0 || T > cfg->max_tokens) return EP_ERR_INVALID_ARG;
+  if (T > 0)
+    for (int i = 0; i < n_required; ++i)
+      if (required[i] == nullptr || !aligned16(required[i])) return EP_ERR_INVALID_ARG;
+  for (int i = 0; i < n_optional; ++i)
+    if (optional[i] != nullptr && !aligned16(optional[i])) return EP_ERR_INVALID_ARG;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
+  return EP_OK;
+}
+
+static RankArgs rank_args(const ep_config* cfg, const ep_layout* layout, RankArgs::Op op) {
+  RankArgs a = {};
+  a.op = op;
+  a.slot_of = layout->slot_of;
+  a.rank_slot_of = layout->rank_slot_of;
+  a.T = layout->num_tokens;
+  a.H = cfg->hidden;
+  a.K = cfg->num_topk;
+  a.E = cfg->num_experts;
+  a.R = cfg->num_ranks;
+  return a;
+}
+
+int32_t ep_dispatch_ranks(const ep_config* cfg, const ep_layout* layout,
+                          const void* d_x, const int64_t* d_topk_idx,
+                          const float* d_topk_weights, void* d_rank_x,
+                          int32_t* d_rank_topk_idx, float* d_rank_topk_w,
+                          void* stream) {
+  const void* req[] = {d_x, d_topk_idx, d_rank_x, d_rank_topk_idx};
+  const void* opt[] = {d_topk_weights, d_rank_topk_w};
+  int32_t st = rank_call_ok(cfg, layout, req, 4, opt, 2);
+  if (st != EP_OK) return st;
+  RankArgs a = rank_args(cfg, layout, RankArgs::kDispatch);
+  a.src = d_x;
+  a.dst = d_rank_x;
+  a.topk_idx = d_topk_idx;
+  a.weights = d_topk_weights;
+  a.rank_topk_idx = d_rank_topk_idx;
+  a.rank_topk_w = d_rank_topk_w;
+  return cuda_status(launch_ranks(a, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t ep_expand(const ep_config* cfg, const ep_layout* layout,
+                  const int64_t* d_topk_idx, const void* d_rank_x,
+                  const float* d_rank_topk_w, void* d_recv_x, float* d_recv_w,
+                  void* stream) {
+  const void* req[] = {d_topk_idx, d_rank_x, d_recv_x};
+  const void* opt[] = {d_rank_topk_w, d_recv_w};
+  int32_t st = rank_call_ok(cfg, layout, req, 3, opt, 2);
+  if (st != EP_OK) return st;
+  if ((d_recv_w == nullptr) != (d_rank_topk_w == nullptr)) return EP_ERR_INVALID_ARG;
+  RankArgs a = rank_args(cfg, layout, RankArgs::kExpand);
+  a.src = d_rank_x;
+  a.dst = d_recv_x;
+  a.topk_idx = d_topk_idx;
+  a.rank_topk_w = const_cast<float*>(d_rank_topk_w);
+  a.recv_w = d_recv_w;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_ranks(a, s);
+  if (e == cudaSuccess && cfg->zero_padding)
+    e = launch_zero_padding_bf16(layout->expert_start, layout->expert_end,
+                                 cfg->num_experts, cfg->hidden, d_recv_x, s);
+  return cuda_status(e);
+}
+
+int32_t ep_reduce_ranks(const ep_config* cfg, const ep_layout* layout,
+                        const int64_t* d_topk_idx, const void* d_expert_out,
+                        const float* d_topk_weights, void* d_rank_y, void* stream) {
+  const void* req[] = {d_topk_idx, d_expert_out, d_rank_y};
+  const void* opt[] = {d_topk_weights};
+  int32_t st = rank_call_ok(cfg, layout, req, 3, opt, 1);
+  if (st != EP_OK) return st;
+  RankArgs a = rank_args(cfg, layout, RankArgs::kReduce);
+  a.src = d_expert_out;
+  a.dst = d_rank_y;
+  a.topk_idx = d_topk_idx;
+  a.weights = d_topk_weights;
+  return cuda_status(launch_ranks(a, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t ep_combine_ranks(const ep_config* cfg, const ep_layout* layout,
+                         const void* d_rank_y, void* d_y, void* stream) {
+  const void* req[] = {d_rank_y, d_y};
+  int32_t st = rank_call_ok(cfg, layout, req, 2, nullptr, 0);
+  if (st != EP_OK) return st;
+  if (cfg->num_ranks > kCombineMaxSlots) return EP_ERR_INVALID_ARG;
+  // The unweighted row sum over the token's rank rows, in ascending rank.
+  CombineArgs a;
+  a.expert_out = d_rank_y;
+  a.topk_weights = nullptr;
+  a.slot_of = layout->rank_slot_of;
+  a.T = layout->num_tokens;
+  a.H = cfg->hidden;
+  a.K = cfg->num_ranks;
+  a.y = d_y;
+  return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t ep_check_error(const ep_layout* layout, void* stream) {

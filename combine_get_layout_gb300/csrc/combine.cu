@@ -30,8 +30,8 @@ __global__ void __launch_bounds__(256)
                    const uint4* __restrict__ b1,
                    const float* __restrict__ recv_w,
                    float* __restrict__ combined_w, uint4* __restrict__ y) {
-  __shared__ int32_t s_slot[32];
-  __shared__ float s_w[32];
+  __shared__ int32_t s_slot[kCombineMaxSlots];
+  __shared__ float s_w[kCombineMaxSlots];
   // CTA = (token, slice of the row): few tokens still fill the GPU.
   const int t = blockIdx.x / slices;
   const int slice = blockIdx.x - t * slices;
@@ -41,12 +41,12 @@ __global__ void __launch_bounds__(256)
   const int v0 = slice * per, v1 = min(nvec, v0 + per);
   pdl_wait();
   pdl_launch_dependents();
-  if (tid < K) {
-    const int sl = slot_of[int64_t(t) * K + tid];
-    s_slot[tid] = sl;
-    s_w[tid] = w != nullptr ? w[int64_t(t) * K + tid] : 1.0f;
+  for (int k = tid; k < K; k += blockDim.x) {
+    const int sl = slot_of[int64_t(t) * K + k];
+    s_slot[k] = sl;
+    s_w[k] = w != nullptr ? w[int64_t(t) * K + k] : 1.0f;
     if (combined_w != nullptr && slice == 0)
-      combined_w[int64_t(t) * K + tid] = sl >= 0 ? recv_w[sl] : 0.0f;
+      combined_w[int64_t(t) * K + k] = sl >= 0 ? recv_w[sl] : 0.0f;
   }
   __syncthreads();
 
@@ -174,29 +174,43 @@ __global__ void __launch_bounds__(256)
     const float gf[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),
                          bf16_lo(g.z), bf16_hi(g.z), bf16_lo(g.w), bf16_hi(g.w)};
 #pragma unroll
-    for (int k = 0; k < KB; ++k) {
-      if (k >= K) break;
-      const int sl = s_slot[k];
-      if (sl < 0) continue;
-      const float wk = s_w[k];
-      uint4 o;
-      o.x = pack_bf16x2(wk * gf[0], wk * gf[1]);
-      o.y = pack_bf16x2(wk * gf[2], wk * gf[3]);
-      o.z = pack_bf16x2(wk * gf[4], wk * gf[5]);
-      o.w = pack_bf16x2(wk * gf[6], wk * gf[7]);
-      grad_Y[int64_t(sl) * nvec + v] = o;
+    for (int kb = 0; kb < KB; kb += kCombineKBatch) {
+      if (kb >= K) break;
+      // the batch's expert rows are loaded together, then used
+      uint4 r[kCombineKBatch];
       if (kGradW) {
-        const uint4 r = ld_stream_u4(Y + int64_t(sl) * nvec + v);
-        float p = part[k];
-        p = fmaf(gf[0], bf16_lo(r.x), p);
-        p = fmaf(gf[1], bf16_hi(r.x), p);
-        p = fmaf(gf[2], bf16_lo(r.y), p);
-        p = fmaf(gf[3], bf16_hi(r.y), p);
-        p = fmaf(gf[4], bf16_lo(r.z), p);
-        p = fmaf(gf[5], bf16_hi(r.z), p);
-        p = fmaf(gf[6], bf16_lo(r.w), p);
-        p = fmaf(gf[7], bf16_hi(r.w), p);
-        part[k] = p;
+#pragma unroll
+        for (int j = 0; j < kCombineKBatch; ++j) {
+          const int k = kb + j;
+          const int sl = k < K ? s_slot[k] : -1;
+          r[j] = sl >= 0 ? ld_stream_u4(Y + int64_t(sl) * nvec + v) : make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kCombineKBatch; ++j) {
+        const int k = kb + j;
+        if (k >= K) break;
+        const int sl = s_slot[k];
+        if (sl < 0) continue;
+        const float wk = s_w[k];
+        uint4 o;
+        o.x = pack_bf16x2(wk * gf[0], wk * gf[1]);
+        o.y = pack_bf16x2(wk * gf[2], wk * gf[3]);
+        o.z = pack_bf16x2(wk * gf[4], wk * gf[5]);
+        o.w = pack_bf16x2(wk * gf[6], wk * gf[7]);
+        grad_Y[int64_t(sl) * nvec + v] = o;
+        if (kGradW) {
+          float p = part[k];
+          p = fmaf(gf[0], bf16_lo(r[j].x), p);
+          p = fmaf(gf[1], bf16_hi(r[j].x), p);
+          p = fmaf(gf[2], bf16_lo(r[j].y), p);
+          p = fmaf(gf[3], bf16_hi(r[j].y), p);
+          p = fmaf(gf[4], bf16_lo(r[j].z), p);
+          p = fmaf(gf[5], bf16_hi(r[j].z), p);
+          p = fmaf(gf[6], bf16_lo(r[j].w), p);
+          p = fmaf(gf[7], bf16_hi(r[j].w), p);
+          part[k] = p;
+        }
       }
     }
   }

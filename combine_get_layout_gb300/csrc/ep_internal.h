@@ -35,12 +35,18 @@ TileGeom layout_tiles(int64_t T, int K);
 // 16-byte multiples, as bulk copies need).
 __host__ __device__ inline int padded_experts(int E) { return (E + 3) & ~3; }
 
+// Ranks padded to a multiple of 4 likewise.
+__host__ __device__ inline int padded_ranks(int R) { return (R + 3) & ~3; }
+// Width of a tile-count row: expert counts then rank counts.
+__host__ __device__ inline int count_row_width(int E, int R) {
+  return padded_experts(E) + padded_ranks(R);
+}
+
 // Workspace carved by ep_get_layout (int32 arrays, each 16-byte aligned):
-//   tile_counts [kLayoutMaxTiles * Epad], tile_rank_counts
-//   [kLayoutMaxTiles * R], tile_err [kLayoutMaxTiles].
+//   tile_counts [kLayoutMaxTiles * (Epad + Rpad)] (row c: tile c's expert
+//   counts, then its rank counts), tile_err [kLayoutMaxTiles].
 struct LayoutWorkspace {
   int32_t* tile_counts;
-  int32_t* tile_rank_counts;
   int32_t* tile_err;
 };
 int64_t layout_workspace_bytes(int E, int R);
@@ -54,6 +60,8 @@ struct LayoutArgs {
   int32_t *expert_count, *expert_start, *expert_end, *rank_start;
   int32_t *tokens_per_rank, *slot_of, *src_info, *err;
   uint8_t* is_token_in_rank;
+  // optional rank rows (all set or all null)
+  int32_t *rank_row_start = nullptr, *rank_slot_of = nullptr, *rank_src = nullptr;
 };
 
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream);
@@ -112,6 +120,27 @@ cudaError_t launch_combine_backward(const CombineBackwardArgs& a, cudaStream_t s
 // [expert_end[e], expert_start[e+1])).
 cudaError_t launch_zero_padding_bf16(const int32_t* expert_start, const int32_t* expert_end,
                                      int E, int H, void* rows, cudaStream_t stream);
+
+// Non-expanded stage kernels (csrc/ranks.cu).
+struct RankArgs {
+  enum Op { kDispatch, kExpand, kReduce } op;
+  const void* src;              // x (dispatch), rank_x (expand), expert rows (reduce)
+  void* dst;                    // rank_x (dispatch), recv_x (expand), rank_y (reduce)
+  const int64_t* topk_idx;
+  const float* weights;         // topk_weights (dispatch, reduce) or null
+  const int32_t* slot_of;
+  const int32_t* rank_slot_of;
+  int32_t* rank_topk_idx;       // dispatch output
+  float* rank_topk_w;           // dispatch output / expand input (optional)
+  float* recv_w;                // expand output (optional)
+  int T, H, K, E, R;
+};
+
+cudaError_t launch_ranks(const RankArgs& a, cudaStream_t stream);
+
+// Largest K the combine kernel reads per token (top-k selections, or rank
+// rows when it sums over destination ranks).
+constexpr int kCombineMaxSlots = 64;
 
 // One CTA waiting (bounded) on a barrier nothing completes.
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, int32_t* err, cudaStream_t stream);

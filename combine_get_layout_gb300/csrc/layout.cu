@@ -39,8 +39,7 @@ TileGeom layout_tiles(int64_t T, int K) {
 static int64_t round16(int64_t b) { return (b + 15) & ~int64_t(15); }
 
 int64_t layout_workspace_bytes(int E, int R) {
-  return round16(int64_t(kLayoutMaxTiles) * padded_experts(E) * 4) +
-         round16(int64_t(kLayoutMaxTiles) * R * 4) +
+  return round16(int64_t(kLayoutMaxTiles) * count_row_width(E, R) * 4) +
          round16(int64_t(kLayoutMaxTiles) * 4);
 }
 
@@ -48,9 +47,7 @@ LayoutWorkspace carve_layout_workspace(void* base, int E, int R) {
   char* p = static_cast<char*>(base);
   LayoutWorkspace ws;
   ws.tile_counts = reinterpret_cast<int32_t*>(p);
-  p += round16(int64_t(kLayoutMaxTiles) * padded_experts(E) * 4);
-  ws.tile_rank_counts = reinterpret_cast<int32_t*>(p);
-  p += round16(int64_t(kLayoutMaxTiles) * R * 4);
+  p += round16(int64_t(kLayoutMaxTiles) * count_row_width(E, R) * 4);
   ws.tile_err = reinterpret_cast<int32_t*>(p);
   return ws;
 }
@@ -169,21 +166,20 @@ __device__ __forceinline__ void survey_span(const int64_t* __restrict__ src, int
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kLayoutThreads)
     layout_count_kernel(const int64_t* __restrict__ topk_idx, int T, int K,
-                        int E, int Epad, int R, int tile_tokens,
+                        int E, int R, int tile_tokens,
                         int32_t* __restrict__ tile_counts,
-                        int32_t* __restrict__ tile_rank_counts,
                         int32_t* __restrict__ tile_err,
                         uint8_t* __restrict__ is_token_in_rank) {
   extern __shared__ int32_t smem_i32[];
   __shared__ int32_t s_err;
-  int32_t* hist = smem_i32;            // [Epad]
-  int32_t* rcnt = hist + Epad;         // [R]
-  int32_t* wscr = rcnt + R;            // [kLayoutWarps * 32]
+  const int Wc = count_row_width(E, R);
+  int32_t* hist = smem_i32;                  // [Wc]: experts, then ranks
+  int32_t* rcnt = hist + padded_experts(E);  // [Rpad]
+  int32_t* wscr = hist + Wc;                 // [kLayoutWarps * 32]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   if (tid == 0) s_err = 0;
-  for (int e = tid; e < Epad; e += blockDim.x) hist[e] = 0;
-  for (int r = tid; r < R; r += blockDim.x) rcnt[r] = 0;
+  for (int e = tid; e < Wc; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   pdl_wait();
   pdl_launch_dependents();
@@ -202,10 +198,8 @@ __global__ void __launch_bounds__(kLayoutThreads)
   if (err) atomicOr(&s_err, err);
   __syncthreads();
 
-  for (int e = tid; e < Epad; e += blockDim.x)
-    tile_counts[int64_t(tile) * Epad + e] = hist[e];
-  for (int r = tid; r < R; r += blockDim.x)
-    tile_rank_counts[int64_t(tile) * R + r] = rcnt[r];
+  for (int e = tid; e < Wc; e += blockDim.x)
+    tile_counts[int64_t(tile) * Wc + e] = hist[e];
   if (tid == 0) tile_err[tile] = s_err;
 }
 
@@ -244,32 +238,36 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int32_t* s_warp,
 
 struct AssignSmem {
   // byte offsets into dynamic shared memory
-  int bar, ring, whist, start, base, total, scratch, bytes;
+  int bar, ring, whist, start, base, total, rstart, rbase, rtotal, scratch, bytes;
   int chunk_rows;
 };
 
 // Shared-memory plan of the assign kernel; identical on host and device.
-__host__ __device__ inline AssignSmem assign_smem(int E, int num_tiles) {
-  const int Epad = padded_experts(E);
+__host__ __device__ inline AssignSmem assign_smem(int E, int R, int num_tiles) {
+  const int Epad = padded_experts(E), Rpad = padded_ranks(R);
+  const int Wc = Epad + Rpad;
   AssignSmem s;
   int rows, nbuf;
-  if (num_tiles >= 1 && num_tiles * Epad <= kScanWholeInts) {
+  if (num_tiles >= 1 && num_tiles * Wc <= kScanWholeInts) {
     rows = num_tiles;  // the whole matrix in one bulk copy
     nbuf = 1;
   } else {
-    rows = kScanChunkInts / Epad;
+    rows = kScanChunkInts / Wc;
     if (rows < 1) rows = 1;
     if (num_tiles >= 1 && rows > num_tiles) rows = num_tiles;
     nbuf = 2;
   }
   s.chunk_rows = rows;
   s.bar = 0;                                   // 2 x 8 bytes, padded
-  s.ring = 16;                                 // nbuf x rows x Epad int32
-  s.whist = s.ring + nbuf * rows * Epad * 4;   // kLayoutWarps x E
+  s.ring = 16;                                 // nbuf x rows x Wc int32
+  s.whist = s.ring + nbuf * rows * Wc * 4;     // kLayoutWarps x E
   s.start = s.whist + kLayoutWarps * E * 4;    // E + 1
   s.base = s.start + ((E + 1 + 3) & ~3) * 4;   // E
   s.total = s.base + Epad * 4;                 // E
-  s.scratch = s.total + Epad * 4;              // 32 + 4
+  s.rstart = s.total + Epad * 4;               // R + 1
+  s.rbase = s.rstart + ((R + 1 + 3) & ~3) * 4; // R
+  s.rtotal = s.rbase + Rpad * 4;               // R
+  s.scratch = s.rtotal + Rpad * 4;             // 32 + 4
   s.bytes = s.scratch + 36 * 4;
   return s;
 }
@@ -278,8 +276,8 @@ __global__ void __launch_bounds__(kLayoutThreads)
     layout_assign_kernel(const int64_t* __restrict__ topk_idx, int T, int K,
                          int E, int R, int A, int tile_tokens, int num_tiles,
                          const int32_t* __restrict__ tile_counts,
-                         const int32_t* __restrict__ tile_rank_counts,
                          const int32_t* __restrict__ tile_err,
+                         const uint8_t* __restrict__ is_token_in_rank,
                          int32_t* __restrict__ expert_count,
                          int32_t* __restrict__ expert_start,
                          int32_t* __restrict__ expert_end,
@@ -287,16 +285,23 @@ __global__ void __launch_bounds__(kLayoutThreads)
                          int32_t* __restrict__ tokens_per_rank,
                          int32_t* __restrict__ slot_of,
                          int32_t* __restrict__ src_info,
+                         int32_t* __restrict__ rank_row_start,
+                         int32_t* __restrict__ rank_slot_of,
+                         int32_t* __restrict__ rank_src,
                          int32_t* __restrict__ err) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int Epad = padded_experts(E);
-  const AssignSmem L = assign_smem(E, num_tiles);
+  const int Wc = count_row_width(E, R);
+  const AssignSmem L = assign_smem(E, R, num_tiles);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
   int32_t* ring = reinterpret_cast<int32_t*>(smem + L.ring);
   int32_t* whist = reinterpret_cast<int32_t*>(smem + L.whist);
   int32_t* s_start = reinterpret_cast<int32_t*>(smem + L.start);
   int32_t* s_base = reinterpret_cast<int32_t*>(smem + L.base);
   int32_t* s_total = reinterpret_cast<int32_t*>(smem + L.total);
+  int32_t* s_rstart = reinterpret_cast<int32_t*>(smem + L.rstart);
+  int32_t* s_rbase = reinterpret_cast<int32_t*>(smem + L.rbase);
+  int32_t* s_rtotal = reinterpret_cast<int32_t*>(smem + L.rtotal);
   int32_t* s_scr = reinterpret_cast<int32_t*>(smem + L.scratch);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x;
@@ -307,6 +312,10 @@ __global__ void __launch_bounds__(kLayoutThreads)
   for (int e = tid; e < E; e += blockDim.x) {
     s_base[e] = 0;
     s_total[e] = 0;
+  }
+  for (int r = tid; r < R; r += blockDim.x) {
+    s_rbase[r] = 0;
+    s_rtotal[r] = 0;
   }
   if (tid == 0) {
     mbar_init(&bar[0], 1);
@@ -323,9 +332,9 @@ __global__ void __launch_bounds__(kLayoutThreads)
   auto issue = [&](int ch) {
     const int r0 = ch * rows;
     const int n = min(rows, num_tiles - r0);
-    const uint32_t bytes = uint32_t(n) * uint32_t(Epad) * 4u;
+    const uint32_t bytes = uint32_t(n) * uint32_t(Wc) * 4u;
     mbar_arrive_expect_tx(&bar[ch & 1], bytes);
-    bulk_load(ring + (ch & 1) * rows * Epad, tile_counts + int64_t(r0) * Epad,
+    bulk_load(ring + (ch & 1) * rows * Wc, tile_counts + int64_t(r0) * Wc,
               bytes, &bar[ch & 1]);
   };
   if (tid == 0) {
@@ -372,16 +381,26 @@ __global__ void __launch_bounds__(kLayoutThreads)
     }
     const int r0 = ch * rows;
     const int n = min(rows, num_tiles - r0);
-    const int32_t* buf = ring + (ch & 1) * rows * Epad;
+    const int32_t* buf = ring + (ch & 1) * rows * Wc;
     for (int e = tid; e < E; e += blockDim.x) {
       int b = 0, tot = 0;
       for (int r = 0; r < n; ++r) {
-        const int v = buf[r * Epad + e];
+        const int v = buf[r * Wc + e];
         tot += v;
         b += (r0 + r < tile) ? v : 0;
       }
       s_base[e] += b;
       s_total[e] += tot;
+    }
+    for (int q = tid; q < R; q += blockDim.x) {  // rank columns
+      int b = 0, tot = 0;
+      for (int r = 0; r < n; ++r) {
+        const int v = buf[r * Wc + Epad + q];
+        tot += v;
+        b += (r0 + r < tile) ? v : 0;
+      }
+      s_rbase[q] += b;
+      s_rtotal[q] += tot;
     }
     __syncthreads();
     if (tid == 0 && ch + 2 < nchunks) issue(ch + 2);
@@ -475,17 +494,45 @@ __global__ void __launch_bounds__(kLayoutThreads)
     if (tid == 0) *err = s_scr[33];
   }
 
-  // Tokens per destination rank: rank r summed by CTA r mod gridDim.
-  for (int r = blockIdx.x; r < R; r += gridDim.x) {
-    int s = 0;
-    for (int c = tid; c < num_tiles; c += blockDim.x)
-      s += tile_rank_counts[int64_t(c) * R + r];
+  // Tokens per destination rank (totals of the rank columns).
+  if (tile == 0)
+    for (int r = tid; r < R; r += blockDim.x) tokens_per_rank[r] = s_rtotal[r];
+
+  // Optional rank rows: rank r owns rows [rank_row_start[r],
+  // rank_row_start[r+1]), one per token sent to it, in token order.
+  if (rank_slot_of != nullptr) {
+    const int rper = (R + blockDim.x - 1) / blockDim.x;
+    const int q0 = min(R, tid * rper), q1 = min(R, q0 + rper);
+    int rl = 0;
+    for (int q = q0; q < q1; ++q) rl += s_rtotal[q];
+    int rows_all = 0;
+    int rrun = block_exclusive_scan(rl, s_scr, &rows_all);
+    for (int q = q0; q < q1; ++q) {
+      s_rstart[q] = rrun;
+      rrun += s_rtotal[q];
+    }
+    if (tid == 0) s_rstart[R] = rows_all;
     __syncthreads();
-    if (tid == 0) s_scr[34] = 0;
-    __syncthreads();
-    atomicAdd(&s_scr[34], s);
-    __syncthreads();
-    if (tid == 0) tokens_per_rank[r] = s_scr[34];
+    if (tile == 0)
+      for (int q = tid; q <= R; q += blockDim.x) rank_row_start[q] = s_rstart[q];
+    if (has_tile) {
+      // one warp per rank: ballot over the tile's tokens, 32 at a time
+      const int nt = min(tile_tokens, T - t0);
+      const uint32_t lt = lanemask_lt();
+      for (int q = warp; q < R; q += kLayoutWarps) {
+        int run = s_rstart[q] + s_rbase[q];
+        for (int c0 = 0; c0 < nt; c0 += 32) {
+          const int t = t0 + c0 + lane;
+          const bool in_tile = c0 + lane < nt;
+          const bool flag = in_tile && is_token_in_rank[int64_t(t) * R + q] != 0;
+          const uint32_t m = __ballot_sync(0xffffffffu, flag);
+          const int row = run + __popc(m & lt);
+          if (in_tile) rank_slot_of[int64_t(t) * R + q] = flag ? row : -1;
+          if (flag) rank_src[row] = t;
+          run += __popc(m);
+        }
+      }
+    }
   }
 
   // Alignment padding rows carry no token (one warp per expert at a time).
@@ -498,7 +545,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
 
 static int count_smem(int E, int R, int K) {
   (void)K;
-  return (padded_experts(E) + R + kLayoutWarps * 32) * 4;
+  return (count_row_width(E, R) + kLayoutWarps * 32) * 4;
 }
 
 cudaError_t prepare_layout_kernels() {
@@ -511,27 +558,27 @@ cudaError_t prepare_layout_kernels() {
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
   const int tiles = a.T > 0 ? a.geom.num_tiles : 0;
   const int tt = a.geom.tile_tokens;
-  const int Epad = padded_experts(a.E);
   cudaError_t st;
   if (tiles > 0) {
     st = launch_pdl(layout_count_kernel, dim3(tiles), dim3(kLayoutThreads),
                     count_smem(a.E, a.R, a.K), stream, a.topk_idx, a.T, a.K,
-                    a.E, Epad, a.R, tt, a.ws.tile_counts, a.ws.tile_rank_counts,
-                    a.ws.tile_err, a.is_token_in_rank);
+                    a.E, a.R, tt, a.ws.tile_counts, a.ws.tile_err,
+                    a.is_token_in_rank);
     if (st != cudaSuccess) return st;
   }
   // With no tokens there are no tiles: one CTA still publishes the empty
   // layout (zero counts and offsets).
-  const AssignSmem sm = assign_smem(a.E, tiles);
+  const AssignSmem sm = assign_smem(a.E, a.R, tiles);
   int grid = tiles > 0 ? tiles : 1;
   const int pad_blocks = a.E < kLayoutMaxTiles ? a.E : kLayoutMaxTiles;
   if (tiles > 0 && grid < pad_blocks) grid = pad_blocks;
   return launch_pdl(layout_assign_kernel, dim3(grid), dim3(kLayoutThreads),
                     sm.bytes, stream, a.topk_idx, a.T, a.K, a.E, a.R, a.A, tt,
-                    tiles, a.ws.tile_counts, a.ws.tile_rank_counts,
-                    a.ws.tile_err, a.expert_count, a.expert_start, a.expert_end,
-                    a.rank_start, a.tokens_per_rank, a.slot_of, a.src_info,
-                    a.err);
+                    tiles, a.ws.tile_counts, a.ws.tile_err,
+                    static_cast<const uint8_t*>(a.is_token_in_rank), a.expert_count,
+                    a.expert_start, a.expert_end, a.rank_start, a.tokens_per_rank,
+                    a.slot_of, a.src_info, a.rank_row_start, a.rank_slot_of,
+                    a.rank_src, a.err);
 }
 
 }  // namespace ep

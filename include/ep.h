@@ -108,6 +108,13 @@ typedef struct {
                                 (-1,-1) for alignment padding rows             */
   int32_t *err;              /* [1]   device error word                        */
   void *workspace;           /* ep_layout_workspace_bytes(cfg) bytes           */
+  /* Optional destination-major rows (all three set, or all NULL): rank r
+   * owns rows [rank_row_start[r], rank_row_start[r+1]), one per token sent
+   * to it (a token is sent once to every rank owning one of its experts),
+   * in token order. */
+  int32_t *rank_row_start;   /* [R+1]                                          */
+  int32_t *rank_slot_of;     /* [max_tokens*R] rank row of (t, r), or -1       */
+  int32_t *rank_src;         /* [max_tokens*min(K,R)] token of each rank row   */
   int32_t num_tokens;        /* set by ep_get_layout                           */
   int32_t reserved;
 } ep_layout;
@@ -291,6 +298,61 @@ EP_API int32_t ep_combine_backward(const ep_config *cfg, const ep_layout *layout
                                    const void *d_expert_out,
                                    void *d_grad_expert_out, float *d_grad_w,
                                    void *stream);
+
+/* ---- Non-expanded (destination-major) stage ------------------------------
+ * ("Deep Dive - DeepEP", "Why expert parallelism needs a communication
+ * layer": a token travels once to each selected destination rank and an
+ * optional expansion then makes one slot per expert; "Dispatch: layout,
+ * move, and epilogue": in non-expanded mode a received row is a source token
+ * with its top-k metadata; "GPU Microarchitecture: DeepEP from First
+ * Principles" 2.1 and 1.2: receive buffer -> expert buffer, and on the way
+ * back expert-major -> destination-major -> token-major.)
+ * All four need a layout computed with the rank-row pointers set
+ * (layout->rank_row_start / rank_slot_of / rank_src); rows = rank_row_start[R]
+ * <= ep_rank_rows_capacity(cfg).  bf16 rows; d_topk_idx is the int64 [T, K]
+ * routing the layout was computed from. */
+
+/* Rows the destination-major buffer may need: max_tokens * min(K, R). */
+EP_API int64_t ep_rank_rows_capacity(const ep_config *cfg);
+
+/* rank_x[row(t,r)] = x[t] for every rank r that owns one of token t's
+ * experts.  Per rank row, K entries of metadata: d_rank_topk_idx (int32) =
+ * local expert id e - r*E/R where the token's k-th expert is on rank r, -1
+ * elsewhere; d_rank_topk_w (fp32, optional) = that selection's weight, 0
+ * elsewhere.  Returns EP_OK or an error. */
+EP_API int32_t ep_dispatch_ranks(const ep_config *cfg, const ep_layout *layout,
+                                 const void *d_x, const int64_t *d_topk_idx,
+                                 const float *d_topk_weights, void *d_rank_x,
+                                 int32_t *d_rank_topk_idx, float *d_rank_topk_w,
+                                 void *stream);
+
+/* Expansion: recv_x[slot_of[t,k]] = rank_x[row(t, rank of expert k)] for
+ * every (t,k) that is not an unused (-1) selection; d_recv_w[slot] = d_rank_topk_w[row, k] (both or
+ * neither).  expand(dispatch_ranks(x)) equals ep_dispatch(x) row for row.
+ * cfg->zero_padding clears the alignment gap rows.  Returns EP_OK or an
+ * error. */
+EP_API int32_t ep_expand(const ep_config *cfg, const ep_layout *layout,
+                         const int64_t *d_topk_idx, const void *d_rank_x,
+                         const float *d_rank_topk_w, void *d_recv_x,
+                         float *d_recv_w, void *stream);
+
+/* Per-rank reduction, the destination rank's partial sum before the rows go
+ * back: rank_y[row(t,r), i] = bf16( fold over k ascending whose expert is on
+ * rank r of acc = fmaf(w[t,k], expert_out[slot_of[t,k], i], acc) ), acc from
+ * +0, weight 1 when d_topk_weights is NULL.  The bf16 partial is the extra
+ * rounding of a two-stage reduction ("Combine: reverse routing plus
+ * reduction": 256 + 1 rounds to 256, then 256 - 256 = 0).  Returns EP_OK or
+ * an error. */
+EP_API int32_t ep_reduce_ranks(const ep_config *cfg, const ep_layout *layout,
+                               const int64_t *d_topk_idx, const void *d_expert_out,
+                               const float *d_topk_weights, void *d_rank_y,
+                               void *stream);
+
+/* Token-major sum over destination ranks: y[t,i] = bf16( fold over r
+ * ascending with a row for (t, r) of acc += rank_y[row, i] ), fp32 from +0.
+ * Needs R <= 64.  Returns EP_OK or an error. */
+EP_API int32_t ep_combine_ranks(const ep_config *cfg, const ep_layout *layout,
+                                const void *d_rank_y, void *d_y, void *stream);
 
 /* Synchronises `stream` and returns the status recorded in the layout's
  * device error word (EP_OK if none): routing errors found by ep_get_layout,

@@ -87,6 +87,16 @@ def _declare(L):
     L.oracle_dispatch_backward.argtypes = [_i32, _i32, _i32] + [_p] * 5
     L.oracle_combine_backward.restype = None
     L.oracle_combine_backward.argtypes = [_i32, _i32, _i32] + [_p] * 6
+    L.oracle_rank_layout.restype = None
+    L.oracle_rank_layout.argtypes = [_i32, _i32, _p, _p, _p, _p]
+    L.oracle_dispatch_ranks.restype = None
+    L.oracle_dispatch_ranks.argtypes = [_i32] * 5 + [_p] * 7
+    L.oracle_expand.restype = None
+    L.oracle_expand.argtypes = [_i32] * 5 + [_p] * 7
+    L.oracle_reduce_ranks.restype = None
+    L.oracle_reduce_ranks.argtypes = [_i32] * 5 + [_p] * 6
+    L.oracle_combine_ranks.restype = None
+    L.oracle_combine_ranks.argtypes = [_i32] * 3 + [_p] * 3
     L.oracle_scale_ld.restype = _i64
     L.oracle_scale_ld.argtypes = [_i64]
     L.oracle_scales_to_col_major.restype = None
@@ -340,3 +350,77 @@ def combine_backward(dy, topk_weights, slot_of, cap, expert_out=None,
     lib().oracle_combine_backward(T, H, K, _ptr(D), _ptr(w), _ptr(slot_of), _ptr(Y),
                                   _ptr(gY), _ptr(gw))
     return gY, gw
+
+
+# ---- non-expanded (destination-major) stage -----------------------------------
+
+def rank_layout(lay: dict) -> dict:
+    """Rank rows from the layout's per-rank flags."""
+    itr = _c(lay["is_token_in_rank"], np.uint8)
+    T, R = itr.shape
+    out = dict(rank_row_start=np.zeros(R + 1, np.int32),
+               rank_slot_of=np.zeros((T, R), np.int32),
+               rank_src=np.full(max(T * R, 1), -1, np.int32))
+    lib().oracle_rank_layout(T, R, _ptr(itr), _ptr(out["rank_row_start"]),
+                             _ptr(out["rank_slot_of"]), _ptr(out["rank_src"]))
+    out["rows"] = int(out["rank_row_start"][-1])
+    return out
+
+
+def dispatch_ranks(x, topk_idx, topk_weights, rl: dict, num_experts, fill=0xFFFF):
+    x = _c(x, np.uint16)
+    T, H = x.shape
+    idx = _c(topk_idx, np.int64)
+    K = idx.shape[1]
+    R = rl["rank_slot_of"].shape[1]
+    n = max(rl["rows"], 1)
+    w = None if topk_weights is None else _c(topk_weights, np.float32)
+    rank_x = np.full((n, H), fill, np.uint16)
+    rank_idx = np.full((n, K), -7, np.int32)
+    rank_w = np.full((n, K), np.nan, np.float32)
+    lib().oracle_dispatch_ranks(T, H, K, num_experts, R, _ptr(x), _ptr(idx), _ptr(w),
+                                _ptr(_c(rl["rank_slot_of"], np.int32)), _ptr(rank_x),
+                                _ptr(rank_idx), _ptr(rank_w))
+    return rank_x, rank_idx, rank_w
+
+
+def expand(topk_idx, lay: dict, rl: dict, rank_x, rank_topk_w, num_experts, fill=0xFFFF):
+    idx = _c(topk_idx, np.int64)
+    T, K = idx.shape
+    R = rl["rank_slot_of"].shape[1]
+    rx = _c(rank_x, np.uint16)
+    H = rx.shape[1]
+    rw = None if rank_topk_w is None else _c(rank_topk_w, np.float32)
+    recv_x = np.full((lay["cap"], H), fill, np.uint16)
+    recv_w = np.full(lay["cap"], np.nan, np.float32)
+    lib().oracle_expand(T, H, K, num_experts, R, _ptr(idx),
+                        _ptr(_c(lay["slot_of"], np.int32)),
+                        _ptr(_c(rl["rank_slot_of"], np.int32)), _ptr(rx), _ptr(rw),
+                        _ptr(recv_x), _ptr(recv_w))
+    return recv_x, recv_w
+
+
+def reduce_ranks(topk_idx, lay: dict, rl: dict, expert_out, topk_weights, num_experts,
+                 fill=0xFFFF):
+    idx = _c(topk_idx, np.int64)
+    T, K = idx.shape
+    R = rl["rank_slot_of"].shape[1]
+    Y = _c(expert_out, np.uint16)
+    H = Y.shape[1]
+    w = None if topk_weights is None else _c(topk_weights, np.float32)
+    rank_y = np.full((max(rl["rows"], 1), H), fill, np.uint16)
+    lib().oracle_reduce_ranks(T, H, K, num_experts, R, _ptr(idx),
+                              _ptr(_c(lay["slot_of"], np.int32)),
+                              _ptr(_c(rl["rank_slot_of"], np.int32)), _ptr(Y), _ptr(w),
+                              _ptr(rank_y))
+    return rank_y
+
+
+def combine_ranks(rl: dict, rank_y):
+    so = _c(rl["rank_slot_of"], np.int32)
+    T, R = so.shape
+    ry = _c(rank_y, np.uint16)
+    H = ry.shape[1]
+    y = np.zeros((T, H), np.uint16)
+    lib().oracle_combine_ranks(T, H, R, _ptr(so), _ptr(ry), _ptr(y))
+    return y

@@ -426,3 +426,104 @@ void oracle_combine_backward(int32_t T, int32_t H, int32_t K, const uint16_t *dy
       if (grad_w) grad_w[(int64_t)t * K + k] = Y ? (float)dot : 0.0f;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Non-expanded (destination-major) stage                                    */
+/* ------------------------------------------------------------------------ */
+
+void oracle_rank_layout(int32_t T, int32_t R, const uint8_t *is_token_in_rank,
+                        int32_t *rank_row_start, int32_t *rank_slot_of,
+                        int32_t *rank_src) {
+  rank_row_start[0] = 0;
+  for (int32_t r = 0; r < R; ++r) {
+    int32_t n = 0;
+    for (int32_t t = 0; t < T; ++t) n += is_token_in_rank[(int64_t)t * R + r] != 0;
+    rank_row_start[r + 1] = rank_row_start[r] + n;
+  }
+  for (int32_t r = 0; r < R; ++r) {
+    int32_t row = rank_row_start[r];
+    for (int32_t t = 0; t < T; ++t) {
+      if (is_token_in_rank[(int64_t)t * R + r]) {
+        rank_slot_of[(int64_t)t * R + r] = row;
+        rank_src[row] = t;
+        ++row;
+      } else {
+        rank_slot_of[(int64_t)t * R + r] = -1;
+      }
+    }
+  }
+}
+
+void oracle_dispatch_ranks(int32_t T, int32_t H, int32_t K, int32_t E, int32_t R,
+                           const uint16_t *x, const int64_t *topk_idx,
+                           const float *w, const int32_t *rank_slot_of,
+                           uint16_t *rank_x, int32_t *rank_topk_idx,
+                           float *rank_topk_w) {
+  const int32_t Eg = E / R;
+  for (int32_t t = 0; t < T; ++t)
+    for (int32_t r = 0; r < R; ++r) {
+      int32_t row = rank_slot_of[(int64_t)t * R + r];
+      if (row < 0) continue;
+      memcpy(rank_x + (int64_t)row * H, x + (int64_t)t * H, (size_t)H * sizeof(uint16_t));
+      for (int32_t k = 0; k < K; ++k) {
+        int64_t e = topk_idx[(int64_t)t * K + k];
+        int on_rank = e >= 0 && e / Eg == r;
+        rank_topk_idx[(int64_t)row * K + k] = on_rank ? (int32_t)(e - (int64_t)r * Eg) : -1;
+        if (w && rank_topk_w)
+          rank_topk_w[(int64_t)row * K + k] = on_rank ? w[(int64_t)t * K + k] : 0.0f;
+      }
+    }
+}
+
+void oracle_expand(int32_t T, int32_t H, int32_t K, int32_t E, int32_t R,
+                   const int64_t *topk_idx, const int32_t *slot_of,
+                   const int32_t *rank_slot_of, const uint16_t *rank_x,
+                   const float *rank_topk_w, uint16_t *recv_x, float *recv_w) {
+  const int32_t Eg = E / R;
+  for (int32_t t = 0; t < T; ++t)
+    for (int32_t k = 0; k < K; ++k) {
+      int64_t e = topk_idx[(int64_t)t * K + k];
+      int32_t s = slot_of[(int64_t)t * K + k];
+      if (e < 0 || s < 0) continue;
+      int32_t row = rank_slot_of[(int64_t)t * R + e / Eg];
+      memcpy(recv_x + (int64_t)s * H, rank_x + (int64_t)row * H, (size_t)H * sizeof(uint16_t));
+      if (rank_topk_w && recv_w) recv_w[s] = rank_topk_w[(int64_t)row * K + k];
+    }
+}
+
+void oracle_reduce_ranks(int32_t T, int32_t H, int32_t K, int32_t E, int32_t R,
+                         const int64_t *topk_idx, const int32_t *slot_of,
+                         const int32_t *rank_slot_of, const uint16_t *Y,
+                         const float *w, uint16_t *rank_y) {
+  const int32_t Eg = E / R;
+  for (int32_t t = 0; t < T; ++t)
+    for (int32_t r = 0; r < R; ++r) {
+      int32_t row = rank_slot_of[(int64_t)t * R + r];
+      if (row < 0) continue;
+      for (int32_t i = 0; i < H; ++i) {
+        float acc = 0.0f;
+        for (int32_t k = 0; k < K; ++k) {
+          int64_t e = topk_idx[(int64_t)t * K + k];
+          int32_t s = slot_of[(int64_t)t * K + k];
+          if (e < 0 || s < 0 || e / Eg != r) continue;
+          float wk = w ? w[(int64_t)t * K + k] : 1.0f;
+          acc = fmaf(wk, oracle_bf16_to_f32(Y[(int64_t)s * H + i]), acc);
+        }
+        rank_y[(int64_t)row * H + i] = oracle_f32_to_bf16(acc);
+      }
+    }
+}
+
+void oracle_combine_ranks(int32_t T, int32_t H, int32_t R,
+                          const int32_t *rank_slot_of, const uint16_t *rank_y,
+                          uint16_t *y) {
+  for (int32_t t = 0; t < T; ++t)
+    for (int32_t i = 0; i < H; ++i) {
+      float acc = 0.0f;
+      for (int32_t r = 0; r < R; ++r) {
+        int32_t row = rank_slot_of[(int64_t)t * R + r];
+        if (row >= 0) acc = acc + oracle_bf16_to_f32(rank_y[(int64_t)row * H + i]);
+      }
+      y[(int64_t)t * H + i] = oracle_f32_to_bf16(acc);
+    }
+}

@@ -150,6 +150,47 @@ void oracle_combine_backward(int32_t T, int32_t H, int32_t K, const uint16_t *dy
                              const float *w, const int32_t *slot_of,
                              const uint16_t *Y, uint16_t *grad_Y, float *grad_w);
 
+/* ---- non-expanded (destination-major) stage ("Deep Dive - DeepEP",
+ * "Why expert parallelism needs a communication layer": a token travels
+ * once to each selected destination rank, an optional expansion then makes
+ * one slot per expert; "Dispatch: layout, move, and epilogue": in
+ * non-expanded mode one received row is a source token with its top-k
+ * metadata; "GPU Microarchitecture: DeepEP from First Principles" 2.1 and
+ * 1.2: receive buffer -> expert buffer, and expert-major -> destination-
+ * major -> token-major on the way back) ------------------------------- */
+/* Rank rows: rank r owns rows [rank_row_start[r], rank_row_start[r+1]),
+ * one per token sent to it, in token order.  rank_slot_of[t*R + r] = row or
+ * -1; rank_src[row] = t.  Uses the flags of oracle_layout. */
+void oracle_rank_layout(int32_t T, int32_t R, const uint8_t *is_token_in_rank,
+                        int32_t *rank_row_start, int32_t *rank_slot_of,
+                        int32_t *rank_src);
+/* rank_x[row(t,r)] = x[t] (bf16 bits); per row, for each k: local expert id
+ * (e - r*E/R) when expert e of (t,k) is on rank r, else -1; its weight there,
+ * else 0 (w may be NULL: weights not written). */
+void oracle_dispatch_ranks(int32_t T, int32_t H, int32_t K, int32_t E, int32_t R,
+                           const uint16_t *x, const int64_t *topk_idx,
+                           const float *w, const int32_t *rank_slot_of,
+                           uint16_t *rank_x, int32_t *rank_topk_idx,
+                           float *rank_topk_w);
+/* Expansion: recv_x[slot_of[t,k]] = rank_x[rank_slot_of[t, r(e)]] for every
+ * unmasked (t,k), r(e) = e / (E/R); recv_w[slot] = rank_topk_w[row, k]. */
+void oracle_expand(int32_t T, int32_t H, int32_t K, int32_t E, int32_t R,
+                   const int64_t *topk_idx, const int32_t *slot_of,
+                   const int32_t *rank_slot_of, const uint16_t *rank_x,
+                   const float *rank_topk_w, uint16_t *recv_x, float *recv_w);
+/* Per-rank reduction (the destination rank's partial sum before sending
+ * back): rank_y[row(t,r), i] = bf16( fold over k ascending with r(e_k) = r of
+ * acc = fmaf(w[t,k], Y[slot_of[t,k], i], acc) ), acc0 = +0, w NULL -> 1. */
+void oracle_reduce_ranks(int32_t T, int32_t H, int32_t K, int32_t E, int32_t R,
+                         const int64_t *topk_idx, const int32_t *slot_of,
+                         const int32_t *rank_slot_of, const uint16_t *Y,
+                         const float *w, uint16_t *rank_y);
+/* Token-major sum over destination ranks: y[t,i] = bf16( fold over r
+ * ascending with rank_slot_of[t,r] >= 0 of acc += rank_y[row, i] ). */
+void oracle_combine_ranks(int32_t T, int32_t H, int32_t R,
+                          const int32_t *rank_slot_of, const uint16_t *rank_y,
+                          uint16_t *y);
+
 #ifdef __cplusplus
 }
 #endif

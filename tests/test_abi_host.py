@@ -43,9 +43,9 @@ def test_library_exports_every_declared_symbol(ep):
 
 
 def test_struct_layouts_match_header(ep):
-    # 8 int32 fields; 10 pointers + 2 int32
+    # 8 int32 fields; 13 pointers + 2 int32
     assert ctypes.sizeof(ep.EpConfig) == 32
-    assert ctypes.sizeof(ep.EpLayout) == 10 * 8 + 8
+    assert ctypes.sizeof(ep.EpLayout) == 13 * 8 + 8
 
 
 def test_capacity_and_workspace(ep):
@@ -95,7 +95,7 @@ def test_null_and_misaligned_pointers_rejected(ep):
     assert ep.ep_get_layout(cfg, 4, None, lay, None, None) == ep.EP_ERR_INVALID_ARG
     # fake, never dereferenced addresses: one misaligned
     fake = [0x10000 + 0x100 * i for i in range(10)]
-    lay = ep.EpLayout(*fake, 0, 0)
+    lay = ep.EpLayout(*fake, None, None, None, 0, 0)
     lay.slot_of = 0x10008
     assert ep.ep_get_layout(cfg, 4, 0x20000, lay, None, None) == ep.EP_ERR_INVALID_ARG
     lay.slot_of = 0x10600
