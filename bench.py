@@ -114,6 +114,10 @@ KERNEL_SOURCES = {
     "dispatch_bf16_kernel": "combine_get_layout_gb300/csrc/dispatch.cu",
     "dispatch_fp8_kernel": "combine_get_layout_gb300/csrc/dispatch.cu",
     "combine_kernel": "combine_get_layout_gb300/csrc/combine.cu",
+    "combine_backward_kernel": "combine_get_layout_gb300/csrc/combine.cu",
+    "dispatch_ranks_kernel": "combine_get_layout_gb300/csrc/ranks.cu",
+    "expand_kernel": "combine_get_layout_gb300/csrc/ranks.cu",
+    "reduce_ranks_kernel": "combine_get_layout_gb300/csrc/ranks.cu",
 }
 
 
@@ -623,7 +627,9 @@ def run_ours(args):
     dom = max(streaming, key=lambda n: avg[n])
     dom_kernel = kernels[dom]
     achieved = gbs[dom]
-    traffic = profiled_traffic(dom_kernel, wl.name) if args.pass_ == "forward" else None
+    # the profile key names the pass when it is not the forward one
+    traffic = profiled_traffic(dom_kernel, wl.name if args.pass_ == "forward"
+                               else f"{wl.name}:{args.pass_}")
     roofline = {"bound": "hbm", "kernel": dom_kernel, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"

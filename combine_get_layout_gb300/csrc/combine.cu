@@ -30,8 +30,10 @@ __global__ void __launch_bounds__(256)
                    const uint4* __restrict__ b1,
                    const float* __restrict__ recv_w,
                    float* __restrict__ combined_w, uint4* __restrict__ y) {
+  // the token's used selections, compacted in ascending k
   __shared__ int32_t s_slot[kCombineMaxSlots];
   __shared__ float s_w[kCombineMaxSlots];
+  __shared__ int s_cnt;
   // CTA = (token, slice of the row): few tokens still fill the GPU.
   const int t = blockIdx.x / slices;
   const int slice = blockIdx.x - t * slices;
@@ -41,33 +43,45 @@ __global__ void __launch_bounds__(256)
   const int v0 = slice * per, v1 = min(nvec, v0 + per);
   pdl_wait();
   pdl_launch_dependents();
-  for (int k = tid; k < K; k += blockDim.x) {
-    const int sl = slot_of[int64_t(t) * K + k];
-    s_slot[k] = sl;
-    s_w[k] = w != nullptr ? w[int64_t(t) * K + k] : 1.0f;
-    if (combined_w != nullptr && slice == 0)
-      combined_w[int64_t(t) * K + k] = sl >= 0 ? recv_w[sl] : 0.0f;
+  if (tid < 32) {
+    // warp 0 reads the route and compacts the used selections (a sparse
+    // route -- e.g. a token's few ranks out of many -- then costs one batch
+    // of loads, not one per group of eight entries)
+    const uint32_t lt = lanemask_lt();
+    int n = 0;
+    for (int c0 = 0; c0 < K; c0 += 32) {
+      const int k = c0 + tid;
+      const int sl = k < K ? slot_of[int64_t(t) * K + k] : -1;
+      const float wk = k < K && w != nullptr ? w[int64_t(t) * K + k] : 1.0f;
+      const uint32_t m = __ballot_sync(0xffffffffu, sl >= 0);
+      if (sl >= 0) {
+        const int pos = n + __popc(m & lt);
+        s_slot[pos] = sl;
+        s_w[pos] = wk;
+      }
+      if (k < K && combined_w != nullptr && slice == 0)
+        combined_w[int64_t(t) * K + k] = sl >= 0 ? recv_w[sl] : 0.0f;
+      n += __popc(m);
+    }
+    if (tid == 0) s_cnt = n;
   }
   __syncthreads();
+  const int cnt = s_cnt;
 
   for (int v = v0 + tid; v < v1; v += blockDim.x) {
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (int kb = 0; kb < K; kb += kCombineKBatch) {
+    for (int kb = 0; kb < cnt; kb += kCombineKBatch) {
       uint4 r[kCombineKBatch];
 #pragma unroll
-      for (int j = 0; j < kCombineKBatch; ++j) {
-        const int k = kb + j;
-        const int sl = k < K ? s_slot[k] : -1;
-        r[j] = sl >= 0 ? ld_stream_u4(Y + int64_t(sl) * nvec + v)
-                       : make_uint4(0, 0, 0, 0);
-      }
+      for (int j = 0; j < kCombineKBatch; ++j)
+        r[j] = kb + j < cnt ? ld_stream_u4(Y + int64_t(s_slot[kb + j]) * nvec + v)
+                            : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int j = 0; j < kCombineKBatch; ++j) {
-        const int k = kb + j;
-        if (k >= K || s_slot[k] < 0) continue;
-        const float wk = s_w[k];
+        if (kb + j >= cnt) break;
+        const float wk = s_w[kb + j];
         acc[0] = fmaf(wk, bf16_lo(r[j].x), acc[0]);
         acc[1] = fmaf(wk, bf16_hi(r[j].x), acc[1]);
         acc[2] = fmaf(wk, bf16_lo(r[j].y), acc[2]);

@@ -16,14 +16,16 @@ namespace ep {
 // ---------------------------------------------------------------------------
 // bf16: bit copies with 16-byte vectors
 // ---------------------------------------------------------------------------
-// One CTA per token; thread v owns the 16-byte vector v of the row (8
+// One CTA per token, or two when the row has more than 512 vectors (two
+// smaller CTAs per SM slot overlap one's route read with the other's
+// stream); each thread owns one 16-byte vector of the row at a time (8
 // channels): one load, then one store per selected expert.  The first load is
 // issued before the route is read, so the two latencies overlap.  (A variant
 // that staged whole rows in shared memory through a ring of bulk copies --
 // one load and K bulk stores per token -- measured ~10% slower on GB300 at
 // the DeepSeek-V3 prefill shape: the register path keeps more stores in
 // flight per SM.)
-__global__ void __launch_bounds__(1024)
+__global__ void __launch_bounds__(512)
     dispatch_bf16_kernel(const uint4* __restrict__ x,
                          const float* __restrict__ w,
                          const int32_t* __restrict__ slot_of, int nvec, int K,
@@ -35,17 +37,18 @@ __global__ void __launch_bounds__(1024)
   pdl_wait();
   pdl_launch_dependents();
   const uint4* row = x + int64_t(t) * nvec;
+  const int v0 = first_vec();
   uint4 first = make_uint4(0, 0, 0, 0);
-  if (tid < nvec) first = ld_stream_u4(row + tid);
+  if (v0 < nvec) first = ld_stream_u4(row + v0);
   if (tid < K) {
     const int sl = slot_of[int64_t(t) * K + tid];
     s_slot[tid] = sl;
-    if (sl >= 0 && w != nullptr && recv_w != nullptr)
+    if (sl >= 0 && w != nullptr && recv_w != nullptr && blockIdx.y == 0)
       recv_w[sl] = w[int64_t(t) * K + tid];
   }
   __syncthreads();
-  for (int v = tid; v < nvec; v += blockDim.x) {
-    const uint4 r = v == tid ? first : ld_stream_u4(row + v);
+  for (int v = v0; v < nvec; v += vec_stride()) {
+    const uint4 r = v == v0 ? first : ld_stream_u4(row + v);
     for (int k = 0; k < K; ++k) {
       const int sl = s_slot[k];
       if (sl >= 0) recv_x[int64_t(sl) * nvec + v] = r;
@@ -244,8 +247,10 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
   if (a.T > 0) {
     if (!a.fp8) {
       const int nvec = a.H / 8;
-      st = launch_pdl(dispatch_bf16_kernel, dim3(a.T), dim3(threads_for(nvec)), 0,
-                      stream, static_cast<const uint4*>(a.x), a.topk_weights,
+      dim3 block;
+      int parts;
+      split_row(nvec, 512, &block, &parts);
+      st = launch_pdl(dispatch_bf16_kernel, dim3(a.T, parts), block, 0, stream, static_cast<const uint4*>(a.x), a.topk_weights,
                       a.slot_of, nvec, a.K, static_cast<uint4*>(a.recv_x), a.recv_w);
     } else if (a.x_q == nullptr) {
       auto kern = a.scale_col_major ? dispatch_fp8_kernel<true> : dispatch_fp8_kernel<false>;

@@ -138,6 +138,17 @@ struct RankArgs {
 
 cudaError_t launch_ranks(const RankArgs& a, cudaStream_t stream);
 
+// Threads per CTA and CTAs per token (grid.y) for a row of nvec vectors: the
+// fewest CTAs of at most `cap` threads, balanced, in whole warps.  Several
+// CTAs per token let one CTA's short per-token preamble overlap another's
+// stream on the same SM.
+inline void split_row(int nvec, int cap, dim3* block, int* parts) {
+  const int p = nvec > 0 ? (nvec + cap - 1) / cap : 1;
+  const int per = (nvec + p - 1) / p;
+  *block = dim3(((per + 31) / 32) * 32);
+  *parts = p;
+}
+
 // Largest K the combine kernel reads per token (top-k selections, or rank
 // rows when it sums over destination ranks).
 constexpr int kCombineMaxSlots = 64;
