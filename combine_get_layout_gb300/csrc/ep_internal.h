@@ -21,6 +21,11 @@ constexpr int kMinTilePairs = 256;
 // through two buffers of kScanChunkInts entries.
 constexpr int kScanWholeInts = 40960;
 constexpr int kScanChunkInts = 8192;
+// Inputs of at most kSmallLayoutPairs (t, k) pairs, with at most
+// kSmallLayoutMaxExperts experts, take the one-launch layout.
+constexpr int kSmallLayoutPairs = 4096;
+constexpr int kSmallLayoutMaxExperts = 2048;
+bool layout_is_small(int64_t T, int K, int E);
 
 
 struct TileGeom {

@@ -4,7 +4,9 @@
 // - DeepEP", "Dispatch: layout, move, and epilogue", and rows ordered by
 // source-global order ("EPHandle: route metadata with a lifetime").
 //
-// Two launches, no inter-CTA waiting:
+// Small inputs (T * K <= kSmallLayoutPairs): one launch in which every CTA
+// surveys the whole input (layout_small_kernel below).  Otherwise two
+// launches, no inter-CTA waiting:
 //   1. count  (one CTA per token tile): validate topk_idx, per-tile expert
 //      histogram with warp-aggregated shared-memory atomics, per-rank dedup
 //      flags and per-tile rank counts.
@@ -96,8 +98,9 @@ constexpr int kSurveyUnroll = 4;
 // the pairs [base, base + TPS*K) of the tile (lanes past `pe` or past the
 // step hold e = -1).  Counts experts into `hist` (leader lanes only; atomics
 // when several warps share it), flags an expert repeated within a token, and
-// writes the tokens' destination-rank rows and per-rank token counts.
-// `sr` is this warp's 32-int shared scratch.  All lanes call.
+// writes the tokens' destination-rank rows (unless itr_tile is null) and
+// per-rank token counts.  `sr` is this warp's 32-int shared scratch.  All
+// lanes call.
 template <bool kSharedHist>
 __device__ __forceinline__ void survey_step(int e, int lane, int base, int pe, int K,
                                             int TPS, int Eg, int R, int32_t* hist,
@@ -121,14 +124,13 @@ __device__ __forceinline__ void survey_step(int e, int lane, int base, int pe, i
       uint64_t mask = 0;
       for (int k = 0; k < K; ++k)
         if (mine[k] >= 0) mask |= uint64_t(1) << mine[k];
-      write_rank_row(itr_tile + int64_t(tl) * R, R, mask);
+      if (itr_tile != nullptr) write_rank_row(itr_tile + int64_t(tl) * R, R, mask);
       for (uint64_t m = mask; m; m &= m - 1) atomicAdd(&s_rank[__ffsll(m) - 1], 1);
     } else {
-      uint8_t* row = itr_tile + int64_t(tl) * R;
       for (int r = 0; r < R; ++r) {
         int in = 0;
         for (int k = 0; k < K; ++k) in |= mine[k] == r;
-        row[r] = static_cast<uint8_t>(in);
+        if (itr_tile != nullptr) itr_tile[int64_t(tl) * R + r] = static_cast<uint8_t>(in);
         if (in) atomicAdd(&s_rank[r], 1);
       }
     }
@@ -543,6 +545,229 @@ __global__ void __launch_bounds__(kLayoutThreads)
 }
 
 
+// ---------------------------------------------------------------------------
+// small inputs: one launch
+// ---------------------------------------------------------------------------
+// When T * K is small (decode batches), the two-launch path is all latency.
+// Here every CTA surveys the whole input itself, one token per thread --
+// counts of the tokens before its own range, within it and after it -- so
+// that no CTA waits for another; then the same aligned scan as the assign
+// kernel, rows for its own few tokens in (t, k) order, rank rows and
+// padding.  The rows are the same as the two-launch path's.
+struct SmallSmem {
+  int idx, hist, start, total, base, rcnt, rstart, scr, bytes;
+};
+
+__host__ __device__ inline SmallSmem small_smem(int E, int R) {
+  const int Epad = padded_experts(E), Rpad = padded_ranks(R);
+  SmallSmem s;
+  int o = 0;
+  s.idx = o;    o += kSmallLayoutPairs * 4;        // the routes, checked, as int32
+  s.hist = o;   o += 3 * Epad * 4;                 // counts: earlier, own, later tokens
+  s.start = o;  o += ((E + 1 + 3) & ~3) * 4;
+  s.total = o;  o += Epad * 4;
+  s.base = o;   o += Epad * 4;                     // next row of each expert
+  s.rcnt = o;   o += 3 * Rpad * 4;                 // rank counts, same regions
+  s.rstart = o; o += ((R + 1 + 3) & ~3) * 4;
+  s.scr = o;    o += 36 * 4;                       // scan scratch, [33] = errors
+  s.bytes = o;
+  return s;
+}
+
+// CTAs of the one-launch layout (each owns about T / kSmallLayoutCtas tokens).
+constexpr int kSmallLayoutCtas = kLayoutMaxTiles;
+
+__global__ void __launch_bounds__(kLayoutThreads)
+    layout_small_kernel(const int64_t* __restrict__ topk_idx, int T, int K, int E,
+                        int R, int A, uint8_t* __restrict__ is_token_in_rank,
+                        int32_t* __restrict__ expert_count,
+                        int32_t* __restrict__ expert_start,
+                        int32_t* __restrict__ expert_end,
+                        int32_t* __restrict__ rank_start,
+                        int32_t* __restrict__ tokens_per_rank,
+                        int32_t* __restrict__ slot_of,
+                        int32_t* __restrict__ src_info,
+                        int32_t* __restrict__ rank_row_start,
+                        int32_t* __restrict__ rank_slot_of,
+                        int32_t* __restrict__ rank_src,
+                        int32_t* __restrict__ err) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int Epad = padded_experts(E), Rpad = padded_ranks(R);
+  const SmallSmem L = small_smem(E, R);
+  int32_t* s_idx = reinterpret_cast<int32_t*>(smem + L.idx);      // [T * K]
+  int32_t* hist = reinterpret_cast<int32_t*>(smem + L.hist);      // [3][Epad]
+  int32_t* s_start = reinterpret_cast<int32_t*>(smem + L.start);
+  int32_t* s_total = reinterpret_cast<int32_t*>(smem + L.total);
+  int32_t* s_base = reinterpret_cast<int32_t*>(smem + L.base);
+  int32_t* rcnt = reinterpret_cast<int32_t*>(smem + L.rcnt);      // [3][Rpad]
+  int32_t* s_rstart = reinterpret_cast<int32_t*>(smem + L.rstart);
+  int32_t* s_scr = reinterpret_cast<int32_t*>(smem + L.scr);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int2* src_info2 = reinterpret_cast<int2*>(src_info);
+
+  for (int i = tid; i < 3 * Epad; i += blockDim.x) hist[i] = 0;
+  for (int i = tid; i < 3 * Rpad; i += blockDim.x) rcnt[i] = 0;
+  if (tid == 0) s_scr[33] = 0;
+  __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // The whole input, range-checked (an id outside [-1, E) is reported and
+  // read as -1), in shared memory: one pass of independent loads.
+  int errbits = 0;
+#pragma unroll 4
+  for (int i = tid; i < T * K; i += blockDim.x) s_idx[i] = read_expert(topk_idx + i, E, errbits);
+  __syncthreads();
+
+  // This CTA's tokens [ctb, cte).
+  const int tt = (T + gridDim.x - 1) / gridDim.x;
+  const int ctb = min(T, int(blockIdx.x) * tt), cte = min(T, ctb + tt);
+  const int Eg = E / R;
+
+  // Survey, one token per thread: repeat checks, the token's destination
+  // ranks (counted once each), expert counts per region (warp-aggregated:
+  // lanes with the same expert and region add once).
+  for (int t0 = 0; t0 < T; t0 += blockDim.x) {
+    const int t = t0 + tid;
+    const bool live = t < T;
+    const int region = t < ctb ? 0 : (t < cte ? 1 : 2);
+    int32_t* h = hist + region * Epad;
+    int32_t* rc = rcnt + region * Rpad;
+    uint64_t mask = 0;
+    if (live && region == 1 && R > 64)   // wide rows: cleared, then set per rank
+      for (int r = 0; r < R; ++r) is_token_in_rank[int64_t(t) * R + r] = 0;
+    const int32_t* row = s_idx + t * K;
+    for (int k = 0; k < K; ++k) {
+      const int e = live ? row[k] : -1;
+      if (e >= 0) {
+        for (int j = 0; j < k; ++j)
+          if (row[j] == e) errbits |= ERRBIT_DUP_EXPERT;
+      }
+      const int key = e >= 0 ? e * 3 + region : -1 - lane;
+      const uint32_t peers = __match_any_sync(0xffffffffu, key);
+      if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&h[e], __popc(peers));
+      if (e >= 0) {
+        const int r = e / Eg;
+        if (R <= 64) {
+          mask |= uint64_t(1) << r;
+        } else {
+          // a rank counted at its first selection in k order
+          bool first = true;
+          for (int j = 0; j < k; ++j)
+            if (row[j] >= 0 && row[j] / Eg == r) first = false;
+          if (first) {
+            atomicAdd(&rc[r], 1);
+            if (region == 1) is_token_in_rank[int64_t(t) * R + r] = 1;
+          }
+        }
+      }
+    }
+    if (live && R <= 64) {
+      for (uint64_t m = mask; m; m &= m - 1) atomicAdd(&rc[__ffsll(m) - 1], 1);
+      if (region == 1) write_rank_row(is_token_in_rank + int64_t(t) * R, R, mask);
+    }
+  }
+  if (errbits) atomicOr(&s_scr[33], errbits);
+  __syncthreads();
+
+  // Per-expert totals, then the aligned exclusive scan over experts.
+  for (int e = tid; e < E; e += blockDim.x)
+    s_total[e] = hist[e] + hist[Epad + e] + hist[2 * Epad + e];
+  __syncthreads();
+  const int per = (E + blockDim.x - 1) / blockDim.x;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int local = 0;
+  for (int e = e0; e < e1; ++e) local += (s_total[e] + A - 1) / A * A;
+  int used = 0;
+  int run = block_exclusive_scan(local, s_scr, &used);
+  for (int e = e0; e < e1; ++e) {
+    s_start[e] = run;
+    s_base[e] = run + hist[e];    // after the rows of earlier tokens
+    run += (s_total[e] + A - 1) / A * A;
+  }
+  if (tid == 0) s_start[E] = used;
+  __syncthreads();
+
+  // Rows of this CTA's tokens (warp 0, 32 pairs a step, in (t, k) order).
+  if (warp == 0) {
+    const int32_t* src = s_idx + ctb * K;
+    const int pe = (cte - ctb) * K;
+    const uint32_t lt = lanemask_lt();
+    for (int b0 = 0; b0 < pe; b0 += 32) {
+      const int p = b0 + lane;
+      const int e = p < pe ? src[p] : -1;
+      const uint32_t peers = __match_any_sync(0xffffffffu, e);
+      int slot = -1;
+      if (e >= 0) slot = s_base[e] + __popc(peers & lt);
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(peers) - 1) s_base[e] += __popc(peers);
+      __syncwarp();
+      if (p < pe) {
+        slot_of[int64_t(ctb) * K + p] = slot;
+        if (slot >= 0) {
+          const int tl = p / K;
+          src_info2[slot] = make_int2(ctb + tl, p - tl * K);
+        }
+      }
+    }
+  }
+
+  // Published per-expert and per-rank arrays (CTA 0, which saw every pair).
+  if (blockIdx.x == 0) {
+    for (int e = tid; e < E; e += blockDim.x) {
+      expert_count[e] = s_total[e];
+      expert_start[e] = s_start[e];
+      expert_end[e] = s_start[e] + s_total[e];
+    }
+    if (tid == 0) {
+      expert_start[E] = s_start[E];
+      *err = s_scr[33];
+    }
+    for (int r = tid; r <= R; r += blockDim.x) rank_start[r] = s_start[r * Eg];
+    for (int r = tid; r < R; r += blockDim.x)
+      tokens_per_rank[r] = rcnt[r] + rcnt[Rpad + r] + rcnt[2 * Rpad + r];
+  }
+
+  // Optional rank rows, in token order within each rank.
+  if (rank_slot_of != nullptr) {
+    const int rper = (R + blockDim.x - 1) / blockDim.x;
+    const int q0 = min(R, tid * rper), q1 = min(R, q0 + rper);
+    int rl = 0;
+    for (int q = q0; q < q1; ++q) rl += rcnt[q] + rcnt[Rpad + q] + rcnt[2 * Rpad + q];
+    int rows_all = 0;
+    int rrun = block_exclusive_scan(rl, s_scr, &rows_all);
+    for (int q = q0; q < q1; ++q) {
+      s_rstart[q] = rrun;
+      rrun += rcnt[q] + rcnt[Rpad + q] + rcnt[2 * Rpad + q];
+    }
+    if (tid == 0) s_rstart[R] = rows_all;
+    __syncthreads();  // also orders this CTA's rank-row bytes before the reads
+    if (blockIdx.x == 0)
+      for (int q = tid; q <= R; q += blockDim.x) rank_row_start[q] = s_rstart[q];
+    const int nt = cte - ctb;
+    const uint32_t lt = lanemask_lt();
+    for (int q = warp; q < R; q += kLayoutWarps) {
+      int rr = s_rstart[q] + rcnt[q];
+      for (int c0 = 0; c0 < nt; c0 += 32) {
+        const int t = ctb + c0 + lane;
+        const bool in_range = c0 + lane < nt;
+        const bool flag = in_range && is_token_in_rank[int64_t(t) * R + q] != 0;
+        const uint32_t m = __ballot_sync(0xffffffffu, flag);
+        const int row = rr + __popc(m & lt);
+        if (in_range) rank_slot_of[int64_t(t) * R + q] = flag ? row : -1;
+        if (flag) rank_src[row] = t;
+        rr += __popc(m);
+      }
+    }
+  }
+
+  // Alignment padding rows carry no token (one warp per expert at a time).
+  for (int e = blockIdx.x * kLayoutWarps + warp; e < E; e += gridDim.x * kLayoutWarps) {
+    const int s0 = s_start[e] + s_total[e], s1 = s_start[e + 1];
+    for (int s = s0 + lane; s < s1; s += 32) src_info2[s] = make_int2(-1, -1);
+  }
+}
+
 static int count_smem(int E, int R, int K) {
   (void)K;
   return (count_row_width(E, R) + kLayoutWarps * 32) * 4;
@@ -551,11 +776,23 @@ static int count_smem(int E, int R, int K) {
 cudaError_t prepare_layout_kernels() {
   const int optin = device_info().max_smem_optin;
   cudaError_t st = allow_max_dynamic_smem(layout_count_kernel, optin);
+  if (st == cudaSuccess) st = allow_max_dynamic_smem(layout_small_kernel, optin);
   if (st != cudaSuccess) return st;
   return allow_max_dynamic_smem(layout_assign_kernel, optin);
 }
 
+bool layout_is_small(int64_t T, int K, int E) {
+  return T * K <= kSmallLayoutPairs && E <= kSmallLayoutMaxExperts;
+}
+
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
+  if (layout_is_small(a.T, a.K, a.E)) {
+    return launch_pdl(layout_small_kernel, dim3(kSmallLayoutCtas), dim3(kLayoutThreads),
+                      small_smem(a.E, a.R).bytes, stream, a.topk_idx, a.T, a.K, a.E, a.R,
+                      a.A, a.is_token_in_rank, a.expert_count, a.expert_start,
+                      a.expert_end, a.rank_start, a.tokens_per_rank, a.slot_of, a.src_info,
+                      a.rank_row_start, a.rank_slot_of, a.rank_src, a.err);
+  }
   const int tiles = a.T > 0 ? a.geom.num_tiles : 0;
   const int tt = a.geom.tile_tokens;
   cudaError_t st;

@@ -121,6 +121,16 @@ MEDIUM = {
     "skew_small": workloads.Workload("skew_small", 700, 512, 64, 6, 8, True,
                                      zipf_alpha=1.2, mask_frac=0.05),
     "many_tiles": workloads.Workload("many_tiles", 70000, 8, 256, 8, 8, False),
+    # more than 64 destination ranks (byte-wise rank rows), both layout paths
+    "wide_ranks_small": workloads.Workload("wide_ranks_small", 100, 128, 256, 8, 128, False,
+                                           expert_alignment=4, mask_frac=0.05),
+    "wide_ranks": workloads.Workload("wide_ranks", 2000, 128, 256, 8, 128, False,
+                                     expert_alignment=4, mask_frac=0.05),
+    # either side of the one-launch layout's limit of 4096 (t, k) pairs
+    "small_edge": workloads.Workload("small_edge", 512, 256, 64, 8, 8, False,
+                                     expert_alignment=16, mask_frac=0.05),
+    "past_small_edge": workloads.Workload("past_small_edge", 513, 256, 64, 8, 8, False,
+                                          expert_alignment=16, mask_frac=0.05),
 }
 
 
@@ -145,9 +155,11 @@ def test_layout_more_tiles_than_target(ep):
     assert_layout_equal(L, oracle_layout(wl, idx, cfg.capacity), wl.num_tokens)
 
 
-def test_layout_hot_expert(ep):
-    """Every token picks expert 0 plus others: one expert holds T rows."""
-    T, E, K = 5000, 32, 4
+@pytest.mark.parametrize("T", [5000, 1000])
+def test_layout_hot_expert(ep, T):
+    """Every token picks expert 0 plus others: one expert holds T rows (both
+    layout paths: 20000 and 4000 (t, k) pairs)."""
+    E, K = 32, 4
     rng = np.random.default_rng(5)
     idx = workloads.random_routes(rng, T, E - 1, K - 1) + 1
     idx = np.concatenate([np.zeros((T, 1), np.int64), idx], axis=1)

@@ -42,6 +42,8 @@ CASES = {
     "ragged": workloads.Workload("ragged", 1000, 1024, 64, 8, 8, False,
                                  expert_alignment=16, mask_frac=0.07),
     "r64": workloads.Workload("r64", 700, 512, 256, 8, 64, False),
+    "r64_small": workloads.Workload("r64_small", 300, 512, 256, 8, 64, False,
+                                    expert_alignment=8, mask_frac=0.05),
     "prefill": workloads.WORKLOADS["prefill"],
     "skew": workloads.WORKLOADS["skew"].with_(use_fp8_dispatch=False),
     "many_tiles": workloads.Workload("many_tiles", 70000, 8, 256, 8, 8, False),
@@ -91,7 +93,7 @@ def test_rank_rows_through_noalloc_entry_point(ep):
     assert np.array_equal(L.rank_src.cpu().numpy()[: rl["rows"]], rl["rank_src"][: rl["rows"]])
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "r64", "skew"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "r64", "r64_small", "skew"])
 def test_dispatch_ranks_and_expand(ep, name):
     wl = CASES[name]
     inp, cfg, L, idx, ora, rl = _setup(ep, wl, zp=True)
@@ -118,7 +120,7 @@ def test_dispatch_ranks_and_expand(ep, name):
     assert torch.equal(recv[:used].view(torch.int16), direct[:used].view(torch.int16))
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "r64", "skew", "prefill"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "r64", "r64_small", "skew", "prefill"])
 @pytest.mark.parametrize("weighted", [True, False])
 def test_reduce_and_combine_ranks(ep, name, weighted):
     wl = CASES[name]
