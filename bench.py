@@ -42,6 +42,9 @@ METRIC = ("dispatch+combine tokens/s and HBM GB/s (% of 8 TB/s) at DeepSeek-V3 "
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20  # twice the GB300's L2
+# (t, k) pairs up to which the layout is one launch (kSmallLayoutPairs in
+# combine_get_layout_gb300/csrc/ep_internal.h); used to count launches
+SMALL_LAYOUT_PAIRS = 4096
 
 
 def log(*a):
@@ -75,6 +78,9 @@ def parse_args():
                         "combine backward (with gate gradients), dispatch backward; "
                         "ranks: layout, dispatch to ranks, expand, reduce to ranks, "
                         "combine over ranks (the non-expanded path)")
+    p.add_argument("--e2e-chunks", type=int, default=8,
+                   help="token chunks of the host-buffer entry points in the e2e leg "
+                        "(copies of later chunks overlap the kernels of earlier ones)")
     p.add_argument("--graph", action="store_true",
                    help="replay each kernel group from a captured CUDA graph "
                         "(removes host launch overhead; for latency-bound sizes)")
@@ -482,8 +488,9 @@ def run_ours(args):
         assert st == 0, ep.ep_status_str(st)
 
     # Stages of one step: (name, callable, kernels launched).  The layout is
-    # count + assign (assign alone when T == 0).
-    lay_launches = 2 if T > 0 else 1
+    # one kernel for at most SMALL_LAYOUT_PAIRS (t, k) pairs, else count +
+    # assign.
+    lay_launches = 1 if T * K <= SMALL_LAYOUT_PAIRS else 2
     one = 1 if T > 0 else 0
     zp_extra = 1 if args.zero_padding else 0
     backward = args.pass_ == "backward"
@@ -664,18 +671,37 @@ def run_ours(args):
             ident = torch.empty((cap, H), dtype=torch.bfloat16, device=device)
         bf_cfg = ep.Config(T, H, K, wl.num_experts, wl.num_ranks, wl.expert_alignment,
                            False, False).c()
+        # The host-buffer entry points move x and y in token chunks overlapped
+        # with the kernels.  They pay off when the rows span two chunks of at
+        # least 4 MiB (below that, copying everything first and launching the
+        # kernels back to back is faster); the epilogue and FP8 input options
+        # have device entry points only, so with those the rows are copied
+        # whole too.
+        host_io = not epilogue and not fp8_opts and T * H * 2 >= 2 * (4 << 20)
+        chunks = args.e2e_chunks
 
         def e2e_step():
-            x_d.copy_(x_h, non_blocking=True)
+            if not host_io:
+                x_d.copy_(x_h, non_blocking=True)
             idx_d.copy_(idx_h, non_blocking=True)
             w_d.copy_(w_h, non_blocking=True)
             layout()
-            dispatch(x_d)
+            if host_io:
+                st = ep.ep_dispatch_from_host(ccfg, L.c, x_h.data_ptr(), p(x_d), p(w_d),
+                                              p(recv_x), p(recv_s), p(recv_w), chunks, sptr)
+                assert st == 0, ep.ep_status_str(st)
+            else:
+                dispatch(x_d)
             if wl.use_fp8_dispatch:
                 st = ep.ep_dispatch(bf_cfg, L.c, p(x_d), None, p(ident), None, None, sptr)
                 assert st == 0
-            combine(ident, y_d)
-            y_h.copy_(y_d, non_blocking=True)
+            if host_io:
+                st = ep.ep_combine_to_host(ccfg, L.c, p(ident), p(w_d), p(y_d), y_h.data_ptr(),
+                                           chunks, sptr)
+                assert st == 0, ep.ep_status_str(st)
+            else:
+                combine(ident, y_d)
+                y_h.copy_(y_d, non_blocking=True)
 
         for _ in range(args.warmup):
             l2_flush()
@@ -696,7 +722,10 @@ def run_ours(args):
         e2e = {"value": T * world / (e_ms / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": x_h.numel() * 2 + idx_h.numel() * 8 + w_h.numel() * 4,
                "d2h_bytes_per_step": y_h.numel() * 2, "ms_per_step": e_ms,
-               "experts": "identity (combine reads the dispatched bf16 rows)"}
+               "experts": "identity (combine reads the dispatched bf16 rows)",
+               "transfer": (f"ep_dispatch_from_host / ep_combine_to_host, {chunks} token "
+                            "chunks (copies overlap the kernels)") if host_io else
+                           "whole-buffer copies on the stream"}
 
     # ---- CPU baseline (rank 0, N = 1) ----------------------------------------
     cpu = None

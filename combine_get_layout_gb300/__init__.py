@@ -49,6 +49,8 @@ ABI_SYMBOLS = (
     "ep_expand",
     "ep_reduce_ranks",
     "ep_combine_ranks",
+    "ep_dispatch_from_host",
+    "ep_combine_to_host",
     "ep_check_error",
     "ep_selftest_wait_timeout",
     "ep_last_cuda_error",
@@ -128,6 +130,11 @@ def _load():
     L.ep_reduce_ranks.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp]
     L.ep_combine_ranks.restype = i32
     L.ep_combine_ranks.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp]
+    L.ep_dispatch_from_host.restype = i32
+    L.ep_dispatch_from_host.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp, vp,
+                                        i32, vp]
+    L.ep_combine_to_host.restype = i32
+    L.ep_combine_to_host.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, i32, vp]
     L.ep_check_error.restype = i32
     L.ep_check_error.argtypes = [P(EpLayout), vp]
     L.ep_selftest_wait_timeout.restype = i32
@@ -234,6 +241,19 @@ def ep_reduce_ranks(cfg, layout, d_topk_idx, d_expert_out, d_topk_weights, d_ran
 def ep_combine_ranks(cfg, layout, d_rank_y, d_y, stream) -> int:
     return int(_lib.ep_combine_ranks(ctypes.byref(cfg), ctypes.byref(layout), d_rank_y,
                                      d_y, stream))
+
+
+def ep_dispatch_from_host(cfg, layout, h_x, d_x, d_topk_weights, d_recv_x, d_recv_scale,
+                          d_recv_w, num_chunks, stream) -> int:
+    return int(_lib.ep_dispatch_from_host(ctypes.byref(cfg), ctypes.byref(layout), h_x, d_x,
+                                          d_topk_weights, d_recv_x, d_recv_scale, d_recv_w,
+                                          int(num_chunks), stream))
+
+
+def ep_combine_to_host(cfg, layout, d_expert_out, d_topk_weights, d_y, h_y, num_chunks,
+                       stream) -> int:
+    return int(_lib.ep_combine_to_host(ctypes.byref(cfg), ctypes.byref(layout), d_expert_out,
+                                       d_topk_weights, d_y, h_y, int(num_chunks), stream))
 
 
 def ep_check_error(layout, stream) -> int:
@@ -405,6 +425,49 @@ def combine(cfg: Config, layout: Layout, expert_out, topk_weights=None, y=None,
                     _ptr(y), _stream(stream))
     _check(st, "ep_combine")
     return y
+
+
+def dispatch_from_host(cfg: Config, layout: Layout, h_x, d_x=None, topk_weights=None,
+                       recv_x=None, recv_scale=None, recv_w=None, want_weights: bool = True,
+                       num_chunks: int = 8, stream=None):
+    """ep_dispatch_from_host.  h_x: bf16 CPU tensor [T, H] (pinned for overlap);
+    d_x: CUDA staging tensor [T, H] (allocated when None).  Returns (recv_x,
+    recv_scale, recv_w, d_x)."""
+    import torch
+
+    cap, H = cfg.capacity, cfg.hidden
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if d_x is None:
+        d_x = torch.empty(tuple(h_x.shape), dtype=torch.bfloat16, device=dev)
+    if recv_x is None:
+        dt = torch.uint8 if cfg.use_fp8_dispatch else torch.bfloat16
+        recv_x = torch.empty((cap, H), dtype=dt, device=dev)
+    if cfg.use_fp8_dispatch and recv_scale is None:
+        recv_scale = torch.empty((cap, H // 128), dtype=torch.float32, device=dev)
+    if want_weights and topk_weights is not None and recv_w is None:
+        recv_w = torch.empty(cap, dtype=torch.float32, device=dev)
+    st = ep_dispatch_from_host(cfg.c(), layout.c, _ptr(h_x), _ptr(d_x), _ptr(topk_weights),
+                               _ptr(recv_x), _ptr(recv_scale), _ptr(recv_w), num_chunks,
+                               _stream(stream))
+    _check(st, "ep_dispatch_from_host")
+    return recv_x, recv_scale, recv_w, d_x
+
+
+def combine_to_host(cfg: Config, layout: Layout, expert_out, topk_weights=None, h_y=None,
+                    d_y=None, num_chunks: int = 8, stream=None):
+    """ep_combine_to_host.  Returns (h_y, d_y): h_y a pinned bf16 CPU tensor
+    [T, H], readable once the stream has been synchronised."""
+    import torch
+
+    T, H = layout.num_tokens, cfg.hidden
+    if h_y is None:
+        h_y = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    if d_y is None:
+        d_y = torch.empty((T, H), dtype=torch.bfloat16, device=expert_out.device)
+    st = ep_combine_to_host(cfg.c(), layout.c, _ptr(expert_out), _ptr(topk_weights), _ptr(d_y),
+                            _ptr(h_y), num_chunks, _stream(stream))
+    _check(st, "ep_combine_to_host")
+    return h_y, d_y
 
 
 def check_error(layout: Layout, stream=None) -> int:

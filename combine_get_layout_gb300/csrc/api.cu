@@ -1,6 +1,8 @@
 // extern "C" entry points of libep_gb300.so (declared in include/ep.h):
 // host-side validation, sizing, and launches on the caller's stream.  The
-// library holds no state besides a per-device property cache.
+// library holds no state besides a per-device property cache and, once the
+// host-buffer entry points have run on a device, that device's copy stream
+// and events.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -235,6 +237,189 @@ int32_t ep_combine(const ep_config* cfg, const ep_layout* layout,
   a.K = cfg->num_topk;
   a.y = d_y;
   return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------------------
+// host buffers: copies in token chunks overlapped with the row kernels
+// ---------------------------------------------------------------------------
+constexpr int kMaxHostChunks = 64;
+
+// One copy stream and kMaxHostChunks + 1 events per device, created by the
+// first host-buffer call on the device and kept until exit.
+struct HostIo {
+  cudaStream_t copy = nullptr;
+  cudaEvent_t ev[kMaxHostChunks + 1] = {};
+};
+
+static cudaError_t host_io(HostIo** out) {
+  static HostIo io[kMaxDevices];
+  static std::once_flag once[kMaxDevices];
+  static cudaError_t result[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  std::call_once(once[dev], [dev] {
+    HostIo& h = io[dev];
+    cudaError_t e = cudaStreamCreateWithFlags(&h.copy, cudaStreamNonBlocking);
+    for (int i = 0; e == cudaSuccess && i <= kMaxHostChunks; ++i)
+      e = cudaEventCreateWithFlags(&h.ev[i], cudaEventDisableTiming);
+    result[dev] = e;
+  });
+  *out = &io[dev];
+  return note_cuda(result[dev]);
+}
+
+// Rows a chunk carries at least: each chunk costs a few µs of copy start-up
+// and cross-stream signalling, which pays off only on copies of several MB.
+constexpr int64_t kMinChunkBytes = int64_t(4) << 20;
+
+// Tokens per chunk: T split into at most `chunks` chunks of at least
+// kMinChunkBytes each, ceil(T / n) tokens a chunk, the last ragged.
+static int chunk_tokens(int T, int chunks, int64_t row_bytes) {
+  int64_t n = int64_t(T) * row_bytes / kMinChunkBytes;
+  if (n > chunks) n = chunks;
+  if (n < 1) n = 1;
+  return int((T + n - 1) / n);
+}
+
+int32_t ep_dispatch_from_host(const ep_config* cfg, const ep_layout* layout,
+                              const void* h_x, void* d_x, const float* d_topk_weights,
+                              void* d_recv_x, float* d_recv_scale, float* d_recv_w,
+                              int32_t num_chunks, void* stream) {
+  if (!config_ok(cfg) || !layout_ptrs_ok(layout)) return EP_ERR_INVALID_ARG;
+  const int T = layout->num_tokens;
+  if (T < 0 || T > cfg->max_tokens) return EP_ERR_INVALID_ARG;
+  if (num_chunks < 1 || num_chunks > kMaxHostChunks) return EP_ERR_INVALID_ARG;
+  if (d_recv_x == nullptr || !aligned16(d_recv_x)) return EP_ERR_INVALID_ARG;
+  if (T > 0 && (h_x == nullptr || d_x == nullptr || !aligned16(d_x)))
+    return EP_ERR_INVALID_ARG;
+  if (d_topk_weights != nullptr && !aligned16(d_topk_weights)) return EP_ERR_INVALID_ARG;
+  if (d_recv_w != nullptr && !aligned16(d_recv_w)) return EP_ERR_INVALID_ARG;
+  if (d_recv_w != nullptr && d_topk_weights == nullptr) return EP_ERR_INVALID_ARG;
+  if (cfg->use_fp8_dispatch && (d_recv_scale == nullptr || !aligned16(d_recv_scale)))
+    return EP_ERR_INVALID_ARG;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
+  HostIo* io = nullptr;
+  if (host_io(&io) != cudaSuccess) return EP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int K = cfg->num_topk;
+  const int64_t row_bytes = int64_t(cfg->hidden) * 2;
+  DispatchArgs base;
+  base.topk_weights = d_topk_weights;
+  base.slot_of = layout->slot_of;
+  base.expert_start = layout->expert_start;
+  base.expert_end = layout->expert_end;
+  base.H = cfg->hidden;
+  base.K = K;
+  base.E = cfg->num_experts;
+  base.fp8 = cfg->use_fp8_dispatch != 0;
+  base.zero_padding = false;
+  base.recv_x = d_recv_x;
+  base.recv_scale = d_recv_scale;
+  base.recv_w = d_recv_w;
+  base.err = layout->err;
+  base.pdl = false;
+  cudaError_t e = cudaSuccess;
+  const int tc = T > 0 ? chunk_tokens(T, num_chunks, row_bytes) : 0;
+  if (T > 0 && tc >= T) {
+    // one chunk: the copy and the kernel in order on the caller's stream
+    e = cudaMemcpyAsync(d_x, h_x, T * row_bytes, cudaMemcpyHostToDevice, s);
+    DispatchArgs a = base;
+    a.x = d_x;
+    a.T = T;
+    if (e == cudaSuccess) e = launch_dispatch(a, s);
+  } else if (T > 0) {
+    const int n_chunks = (T + tc - 1) / tc;
+    // the staging rows are free once the stream's earlier work is done
+    e = cudaEventRecord(io->ev[kMaxHostChunks], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(io->copy, io->ev[kMaxHostChunks], 0);
+    for (int c = 0; e == cudaSuccess && c < n_chunks; ++c) {
+      const int t0 = c * tc, n = T - t0 < tc ? T - t0 : tc;
+      e = cudaMemcpyAsync(static_cast<char*>(d_x) + t0 * row_bytes,
+                          static_cast<const char*>(h_x) + t0 * row_bytes, n * row_bytes,
+                          cudaMemcpyHostToDevice, io->copy);
+      if (e == cudaSuccess) e = cudaEventRecord(io->ev[c], io->copy);
+    }
+    for (int c = 0; e == cudaSuccess && c < n_chunks; ++c) {
+      const int t0 = c * tc, n = T - t0 < tc ? T - t0 : tc;
+      e = cudaStreamWaitEvent(s, io->ev[c], 0);
+      if (e != cudaSuccess) break;
+      DispatchArgs a = base;
+      a.x = static_cast<const char*>(d_x) + t0 * row_bytes;
+      a.topk_weights = d_topk_weights != nullptr ? d_topk_weights + int64_t(t0) * K : nullptr;
+      a.slot_of = layout->slot_of + int64_t(t0) * K;
+      a.T = n;
+      e = launch_dispatch(a, s);
+    }
+  }
+  if (e == cudaSuccess && cfg->zero_padding) {
+    DispatchArgs z = base;
+    z.T = 0;
+    z.zero_padding = true;
+    e = launch_dispatch(z, s);
+  }
+  return cuda_status(e);
+}
+
+int32_t ep_combine_to_host(const ep_config* cfg, const ep_layout* layout,
+                           const void* d_expert_out, const float* d_topk_weights,
+                           void* d_y, void* h_y, int32_t num_chunks, void* stream) {
+  if (!config_ok(cfg) || !layout_ptrs_ok(layout)) return EP_ERR_INVALID_ARG;
+  const int T = layout->num_tokens;
+  if (T < 0 || T > cfg->max_tokens) return EP_ERR_INVALID_ARG;
+  if (num_chunks < 1 || num_chunks > kMaxHostChunks) return EP_ERR_INVALID_ARG;
+  if (T > 0) {
+    if (d_expert_out == nullptr || !aligned16(d_expert_out)) return EP_ERR_INVALID_ARG;
+    if (d_y == nullptr || !aligned16(d_y) || h_y == nullptr) return EP_ERR_INVALID_ARG;
+  }
+  if (d_topk_weights != nullptr && !aligned16(d_topk_weights)) return EP_ERR_INVALID_ARG;
+  if (T == 0) return EP_OK;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
+  HostIo* io = nullptr;
+  if (host_io(&io) != cudaSuccess) return EP_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int K = cfg->num_topk;
+  const int64_t row_bytes = int64_t(cfg->hidden) * 2;
+  const int tc = chunk_tokens(T, num_chunks, row_bytes);
+  const int n_chunks = (T + tc - 1) / tc;
+  cudaError_t e = cudaSuccess;
+  if (n_chunks == 1) {
+    // one chunk: the kernel and the copy in order on the caller's stream
+    CombineArgs a;
+    a.expert_out = d_expert_out;
+    a.topk_weights = d_topk_weights;
+    a.slot_of = layout->slot_of;
+    a.T = T;
+    a.H = cfg->hidden;
+    a.K = K;
+    a.y = d_y;
+    e = launch_combine(a, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(h_y, d_y, T * row_bytes, cudaMemcpyDeviceToHost, s);
+    return cuda_status(e);
+  }
+  for (int c = 0; e == cudaSuccess && c < n_chunks; ++c) {
+    const int t0 = c * tc, n = T - t0 < tc ? T - t0 : tc;
+    CombineArgs a;
+    a.expert_out = d_expert_out;
+    a.topk_weights = d_topk_weights != nullptr ? d_topk_weights + int64_t(t0) * K : nullptr;
+    a.slot_of = layout->slot_of + int64_t(t0) * K;
+    a.T = n;
+    a.H = cfg->hidden;
+    a.K = K;
+    a.y = static_cast<char*>(d_y) + t0 * row_bytes;
+    a.pdl = false;
+    e = launch_combine(a, s);
+    if (e == cudaSuccess) e = cudaEventRecord(io->ev[c], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(io->copy, io->ev[c], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<char*>(h_y) + t0 * row_bytes,
+                          static_cast<const char*>(d_y) + t0 * row_bytes, n * row_bytes,
+                          cudaMemcpyDeviceToHost, io->copy);
+  }
+  // the caller's stream completes only after the last rows reached the host
+  if (e == cudaSuccess) e = cudaEventRecord(io->ev[kMaxHostChunks], io->copy);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, io->ev[kMaxHostChunks], 0);
+  return cuda_status(e);
 }
 
 int64_t ep_scale_ld(const ep_config* cfg) {

@@ -138,13 +138,13 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   const uint4* Y = static_cast<const uint4*>(a.expert_out);
   uint4* y = static_cast<uint4*>(a.y);
   if (nb == 0)
-    return launch_pdl(combine_kernel<0>, grid, block, 0, stream, Y, a.topk_weights,
-                      a.slot_of, a.H, a.K, slices, b0, b1, a.recv_w, a.combined_w, y);
+    return launch_ex(a.pdl, combine_kernel<0>, grid, block, 0, stream, Y, a.topk_weights,
+                     a.slot_of, a.H, a.K, slices, b0, b1, a.recv_w, a.combined_w, y);
   if (nb == 1)
-    return launch_pdl(combine_kernel<1>, grid, block, 0, stream, Y, a.topk_weights,
-                      a.slot_of, a.H, a.K, slices, b0, b1, a.recv_w, a.combined_w, y);
-  return launch_pdl(combine_kernel<2>, grid, block, 0, stream, Y, a.topk_weights,
-                    a.slot_of, a.H, a.K, slices, b0, b1, a.recv_w, a.combined_w, y);
+    return launch_ex(a.pdl, combine_kernel<1>, grid, block, 0, stream, Y, a.topk_weights,
+                     a.slot_of, a.H, a.K, slices, b0, b1, a.recv_w, a.combined_w, y);
+  return launch_ex(a.pdl, combine_kernel<2>, grid, block, 0, stream, Y, a.topk_weights,
+                   a.slot_of, a.H, a.K, slices, b0, b1, a.recv_w, a.combined_w, y);
 }
 
 // ---------------------------------------------------------------------------

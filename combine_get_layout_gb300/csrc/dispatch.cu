@@ -250,21 +250,22 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
       dim3 block;
       int parts;
       split_row(nvec, 512, &block, &parts);
-      st = launch_pdl(dispatch_bf16_kernel, dim3(a.T, parts), block, 0, stream, static_cast<const uint4*>(a.x), a.topk_weights,
-                      a.slot_of, nvec, a.K, static_cast<uint4*>(a.recv_x), a.recv_w);
+      st = launch_ex(a.pdl, dispatch_bf16_kernel, dim3(a.T, parts), block, 0, stream,
+                     static_cast<const uint4*>(a.x), a.topk_weights, a.slot_of, nvec, a.K,
+                     static_cast<uint4*>(a.recv_x), a.recv_w);
     } else if (a.x_q == nullptr) {
       auto kern = a.scale_col_major ? dispatch_fp8_kernel<true> : dispatch_fp8_kernel<false>;
-      st = launch_pdl(kern, dim3(a.T), dim3(threads_for(a.H / 16)), 0, stream,
-                      static_cast<const uint4*>(a.x), a.topk_weights, a.slot_of, a.H,
-                      a.K, a.scale_ld, static_cast<uint8_t*>(a.recv_x), a.recv_scale,
-                      a.recv_w);
+      st = launch_ex(a.pdl, kern, dim3(a.T), dim3(threads_for(a.H / 16)), 0, stream,
+                     static_cast<const uint4*>(a.x), a.topk_weights, a.slot_of, a.H,
+                     a.K, a.scale_ld, static_cast<uint8_t*>(a.recv_x), a.recv_scale,
+                     a.recv_w);
     } else {
       auto kern = a.scale_col_major ? dispatch_fp8_copy_kernel<true>
                                     : dispatch_fp8_copy_kernel<false>;
-      st = launch_pdl(kern, dim3(a.T), dim3(threads_for(a.H / 16)), 0, stream,
-                      reinterpret_cast<const uint4*>(a.x_q), a.x_scale, a.topk_weights,
-                      a.slot_of, a.H, a.K, a.scale_ld, static_cast<uint8_t*>(a.recv_x),
-                      a.recv_scale, a.recv_w);
+      st = launch_ex(a.pdl, kern, dim3(a.T), dim3(threads_for(a.H / 16)), 0, stream,
+                     reinterpret_cast<const uint4*>(a.x_q), a.x_scale, a.topk_weights,
+                     a.slot_of, a.H, a.K, a.scale_ld, static_cast<uint8_t*>(a.recv_x),
+                     a.recv_scale, a.recv_w);
     }
     if (st != cudaSuccess) return st;
   }

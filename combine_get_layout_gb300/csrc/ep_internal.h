@@ -88,6 +88,9 @@ struct DispatchArgs {
   // x, and column-major scales with leading dimension scale_ld.
   const uint8_t* x_q = nullptr;
   const float* x_scale = nullptr;
+  // programmatic dependent launch of the row kernels (off after a wait on
+  // another stream)
+  bool pdl = true;
   bool scale_col_major = false;
   int64_t scale_ld = 0;
 };
@@ -105,6 +108,7 @@ struct CombineArgs {
   const void* bias1 = nullptr;
   const float* recv_w = nullptr;
   float* combined_w = nullptr;
+  bool pdl = true;   // as in DispatchArgs
 };
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
@@ -163,9 +167,11 @@ cudaError_t launch_wait_selftest(uint64_t timeout_ns, int32_t* err, cudaStream_t
 
 // Launches `kernel` with programmatic stream serialisation (see pdl_wait in
 // ep_device.cuh).
+// With pdl = false the launch is an ordinary stream-ordered one (used after
+// a wait on another stream's event, where the kernel must not start early).
 template <typename... Params, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block,
-                       size_t smem, cudaStream_t stream, Args&&... args) {
+cudaError_t launch_ex(bool pdl, void (*kernel)(Params...), dim3 grid, dim3 block,
+                      size_t smem, cudaStream_t stream, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -175,8 +181,14 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block,
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block,
+                       size_t smem, cudaStream_t stream, Args&&... args) {
+  return launch_ex(true, kernel, grid, block, smem, stream, std::forward<Args>(args)...);
 }
 
 // Raises `kernel`'s dynamic shared-memory limit to what the device allows

@@ -354,6 +354,46 @@ EP_API int32_t ep_reduce_ranks(const ep_config *cfg, const ep_layout *layout,
 EP_API int32_t ep_combine_ranks(const ep_config *cfg, const ep_layout *layout,
                                 const void *d_rank_y, void *d_y, void *stream);
 
+/* ---- Host buffers ---------------------------------------------------------
+ * For callers whose token rows live in host memory (CPU-resident activations,
+ * a serving loop that stages batches on the host).  The rows move in token
+ * chunks on a copy stream the library owns, and each chunk's dispatch or
+ * combine waits only for its own chunk's copy ("Deep Dive - DeepEP",
+ * "EventOverlap: a stream contract": streams let data movement and compute
+ * overlap; readiness is a stream dependency on an event, not a host wait).
+ * Results equal ep_dispatch / ep_combine bit for bit.
+ * The first call on a device creates that device's copy stream and events
+ * (kept until exit); calls on one device share them, so their copies run in
+ * call order.  Host buffers should be pinned (page-locked): pageable memory
+ * works but its copies do not overlap.  num_chunks (1..64) is an upper
+ * bound: a chunk carries at least 4 MiB of rows (T rows of 2H bytes split
+ * into n = min(num_chunks, max(1, floor(2HT / 4 MiB))) chunks of
+ * ceil(T / n) tokens, the last ragged); a single chunk is copied on `stream`
+ * itself, with no copy stream involved. */
+
+/* As ep_dispatch with x in host memory: h_x (host bf16 [T, H]) is copied
+ * into d_x (device bf16 [T, H], a staging buffer the caller owns and that
+ * holds x afterwards) chunk by chunk, overlapped with the dispatch of the
+ * chunks already copied.  The copies start once the work enqueued on
+ * `stream` before this call is done (so d_x may still be read by it).
+ * cfg->use_fp8_dispatch and cfg->zero_padding act as in ep_dispatch.
+ * Returns EP_OK or an error. */
+EP_API int32_t ep_dispatch_from_host(const ep_config *cfg, const ep_layout *layout,
+                                     const void *h_x, void *d_x,
+                                     const float *d_topk_weights, void *d_recv_x,
+                                     float *d_recv_scale, float *d_recv_w,
+                                     int32_t num_chunks, void *stream);
+
+/* As ep_combine with y returned to host memory: each chunk of tokens is
+ * combined into d_y (device bf16 [T, H], staging owned by the caller) and
+ * then copied to h_y (host bf16 [T, H]) while later chunks combine.  Work
+ * enqueued on `stream` after this call starts after the last copy, so a
+ * synchronisation of `stream` makes h_y readable.  Returns EP_OK or an
+ * error. */
+EP_API int32_t ep_combine_to_host(const ep_config *cfg, const ep_layout *layout,
+                                  const void *d_expert_out, const float *d_topk_weights,
+                                  void *d_y, void *h_y, int32_t num_chunks, void *stream);
+
 /* Synchronises `stream` and returns the status recorded in the layout's
  * device error word (EP_OK if none): routing errors found by ep_get_layout,
  * and EP_ERR_TIMEOUT if a bounded on-chip wait of a later call gave up. */

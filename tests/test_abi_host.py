@@ -108,6 +108,23 @@ def test_null_and_misaligned_pointers_rejected(ep):
     assert ep.ep_dispatch(cfg, lay, 0x30000, None, 0x40000, None, 0x50000, None) == ep.EP_ERR_INVALID_ARG
     cfg8 = ep.Config(16, 128, 2, 8, 2, 4, use_fp8_dispatch=True).c()
     assert ep.ep_dispatch(cfg8, lay, 0x30000, None, 0x40000, None, None, None) == ep.EP_ERR_INVALID_ARG
+    # host-buffer entry points: chunk count outside 1..64, missing host or
+    # staging buffer, misaligned staging buffer
+    for chunks in (0, 65, -3):
+        assert ep.ep_dispatch_from_host(cfg, lay, 0x60000, 0x30000, None, 0x40000, None, None,
+                                        chunks, None) == ep.EP_ERR_INVALID_ARG
+        assert ep.ep_combine_to_host(cfg, lay, 0x40000, None, 0x30000, 0x60000, chunks,
+                                     None) == ep.EP_ERR_INVALID_ARG
+    assert ep.ep_dispatch_from_host(cfg, lay, None, 0x30000, None, 0x40000, None, None, 4,
+                                    None) == ep.EP_ERR_INVALID_ARG
+    assert ep.ep_dispatch_from_host(cfg, lay, 0x60000, 0x30008, None, 0x40000, None, None, 4,
+                                    None) == ep.EP_ERR_INVALID_ARG
+    assert ep.ep_dispatch_from_host(cfg8, lay, 0x60000, 0x30000, None, 0x40000, None, None, 4,
+                                    None) == ep.EP_ERR_INVALID_ARG
+    assert ep.ep_combine_to_host(cfg, lay, 0x40000, None, 0x30000, None, 4,
+                                 None) == ep.EP_ERR_INVALID_ARG
+    assert ep.ep_combine_to_host(cfg, lay, 0x40000, None, None, 0x60000, 4,
+                                 None) == ep.EP_ERR_INVALID_ARG
 
 
 def test_status_strings(ep):

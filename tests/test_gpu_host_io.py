@@ -1,0 +1,154 @@
+"""GPU checks of the host-buffer entry points (ep_dispatch_from_host,
+ep_combine_to_host): rows copied in token chunks on the library's copy
+stream, each chunk's kernel waiting for its own copy.  The results must equal
+the device-buffer entry points bit for bit (which the parity suite holds to
+the oracle), for one chunk (on the caller's stream) and several (on the copy
+stream) with a ragged last chunk, FP8 rows and zero padding; one case is
+also compared with the oracle directly."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ep():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from conftest import load_build_module
+
+    load_build_module().build()
+    import combine_get_layout_gb300 as ep
+
+    return ep
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def pinned_bf16(u16):
+    return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(
+        torch.bfloat16).pin_memory()
+
+
+def u16(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+CASES = {
+    # 2 MB of rows: one chunk whatever num_chunks is (chunks carry >= 4 MiB)
+    "ragged": workloads.Workload("ragged", 1000, 1024, 64, 8, 8, False,
+                                 expert_alignment=16, mask_frac=0.07),
+    # 35.8 MB of rows: up to 8 chunks, the last ragged
+    "wide": workloads.Workload("wide", 2500, 7168, 64, 8, 8, False,
+                               expert_alignment=16, mask_frac=0.05),
+    "wide_fp8": workloads.Workload("wide_fp8", 2500, 7168, 64, 8, 8, True,
+                                   expert_alignment=16, mask_frac=0.05),
+    "fp8": workloads.Workload("fp8", 333, 1024, 32, 4, 4, True, expert_alignment=8,
+                              mask_frac=0.1),
+    "few_tokens": workloads.Workload("few_tokens", 5, 256, 16, 2, 4, False,
+                                     expert_alignment=4),
+    "prefill": workloads.WORKLOADS["prefill"],
+}
+
+
+def _run(ep, wl, chunks, zp, seed=0):
+    inp = workloads.make_inputs(wl, seed=seed)
+    cfg = ep.Config(wl.num_tokens, wl.hidden, wl.num_topk, wl.num_experts, wl.num_ranks,
+                    wl.expert_alignment, wl.use_fp8_dispatch, zp)
+    L = ep.get_layout(cfg, dev(inp["topk_idx"]), sync=True)
+    w = dev(inp["topk_weights"])
+    x_h = pinned_bf16(inp["x"])
+    x_d = x_h.cuda()
+    ref = ep.dispatch(cfg, L, x_d, w)
+    got_x, got_s, got_w, staged = ep.dispatch_from_host(cfg, L, x_h, topk_weights=w,
+                                                        num_chunks=chunks)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed + 5)
+    Y = torch.randn((cfg.capacity, wl.hidden), generator=g, device="cuda").to(torch.bfloat16)
+    y_ref = ep.combine(cfg, L, Y, w)
+    h_y, _ = ep.combine_to_host(cfg, L, Y, w, num_chunks=chunks)
+    torch.cuda.current_stream().synchronize()
+    return inp, cfg, L, ref, (got_x, got_s, got_w, staged), y_ref, h_y
+
+
+def _rows(L, cfg, zp):
+    es = L.expert_start.cpu().numpy()
+    used = int(es[-1])
+    if zp:
+        return np.arange(used)
+    src = L.src_info.cpu().numpy().reshape(-1, 2)[:used]
+    return np.nonzero(src[:, 0] >= 0)[0]
+
+
+@pytest.mark.parametrize("name,chunks,zp", [
+    ("ragged", 1, False), ("ragged", 8, True), ("fp8", 7, False), ("fp8", 4, True),
+    ("few_tokens", 8, False), ("wide", 3, False), ("wide", 8, True), ("wide", 64, False),
+    ("wide_fp8", 5, False), ("wide_fp8", 8, True), ("prefill", 8, False)])
+def test_host_buffers_equal_device_buffers(ep, name, chunks, zp):
+    wl = CASES[name]
+    inp, cfg, L, ref, got, y_ref, h_y = _run(ep, wl, chunks, zp)
+    rows = torch.from_numpy(_rows(L, cfg, zp)).long().cuda()
+    rx, rs, rw = ref
+    gx, gs, gw, staged = got
+    assert torch.equal(gx[rows].view(torch.uint8), rx[rows].view(torch.uint8))
+    if cfg.use_fp8_dispatch:
+        assert torch.equal(gs[rows].view(torch.int32), rs[rows].view(torch.int32))
+    assert torch.equal(gw[rows].view(torch.int32), rw[rows].view(torch.int32))
+    # the staging buffer holds x afterwards
+    assert np.array_equal(u16(staged), inp["x"])
+    assert np.array_equal(u16(h_y), u16(y_ref))
+
+
+def test_host_dispatch_matches_oracle(ep):
+    wl = CASES["wide"]
+    inp, cfg, L, ref, got, y_ref, h_y = _run(ep, wl, 5, True)
+    ora = oracle.layout(inp["topk_idx"], wl.num_experts, wl.num_ranks, wl.expert_alignment,
+                        cap=cfg.capacity)
+    want_x, want_w = oracle.dispatch_bf16(inp["x"], inp["topk_weights"], ora, zero_padding=True)
+    used = int(ora["expert_start"][-1])
+    assert np.array_equal(u16(got[0])[:used], want_x[:used])
+    rows = ora["src_info"][:used, 0] >= 0
+    assert np.array_equal(got[2].cpu().numpy()[:used][rows], want_w[:used][rows])
+
+
+def test_two_calls_in_a_row_reuse_the_events(ep):
+    """Back-to-back calls with different inputs, no synchronisation between
+    them: each result must be its own call's."""
+    wl = CASES["wide"]
+    outs = []
+    for seed in (0, 1):
+        inp = workloads.make_inputs(wl, seed=seed)
+        cfg = ep.Config(wl.num_tokens, wl.hidden, wl.num_topk, wl.num_experts, wl.num_ranks,
+                        wl.expert_alignment, False, False)
+        L = ep.get_layout(cfg, dev(inp["topk_idx"]), sync=True)
+        w = dev(inp["topk_weights"])
+        x_h = pinned_bf16(inp["x"])
+        recv, _, _, _ = ep.dispatch_from_host(cfg, L, x_h, topk_weights=w, num_chunks=6)
+        h_y, _ = ep.combine_to_host(cfg, L, recv, w, num_chunks=6)
+        outs.append((inp, cfg, L, x_h, w, h_y))
+    torch.cuda.current_stream().synchronize()
+    for inp, cfg, L, x_h, w, h_y in outs:
+        recv, _, _ = ep.dispatch(cfg, L, x_h.cuda(), w)
+        y_ref = ep.combine(cfg, L, recv, w)
+        torch.cuda.synchronize()
+        assert np.array_equal(u16(h_y), u16(y_ref))
+
+
+def test_empty_batch(ep):
+    wl = CASES["few_tokens"]
+    cfg = ep.Config(wl.num_tokens, wl.hidden, wl.num_topk, wl.num_experts, wl.num_ranks,
+                    wl.expert_alignment, False, True)
+    L = ep.get_layout(cfg, torch.zeros((0, wl.num_topk), dtype=torch.int64, device="cuda"),
+                      sync=True)
+    x_h = torch.empty((0, wl.hidden), dtype=torch.bfloat16).pin_memory()
+    recv, _, _, _ = ep.dispatch_from_host(cfg, L, x_h, num_chunks=4)
+    h_y, _ = ep.combine_to_host(cfg, L, recv, num_chunks=4)
+    torch.cuda.synchronize()
+    assert h_y.shape == (0, wl.hidden)
