@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(256)
 }
 
 // CTAs wanted in flight before rows are split across CTAs.
-constexpr int kCombineMinCtas = 2048;
+constexpr int kCombineMinCtas = 8192;
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;

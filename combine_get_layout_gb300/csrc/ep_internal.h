@@ -17,9 +17,10 @@ constexpr int kLayoutWarps = kLayoutThreads / 32;
 constexpr int kLayoutMaxTiles = 152;
 constexpr int kMinTilePairs = 256;
 // The assign kernel loads the whole tile-count matrix with one bulk copy
-// when it has at most kScanWholeInts entries; otherwise it streams it
-// through two buffers of kScanChunkInts entries.
-constexpr int kScanWholeInts = 40960;
+// when it fits, with the kernel's other shared arrays, in kAssignSmemBudget
+// bytes; otherwise it streams it through two buffers of kScanChunkInts
+// entries.
+constexpr int kAssignSmemBudget = 220 * 1024;
 constexpr int kScanChunkInts = 8192;
 // Inputs of at most kSmallLayoutPairs (t, k) pairs, with at most
 // kSmallLayoutMaxExperts experts, take the one-launch layout.

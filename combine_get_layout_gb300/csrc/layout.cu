@@ -249,8 +249,11 @@ __host__ __device__ inline AssignSmem assign_smem(int E, int R, int num_tiles) {
   const int Epad = padded_experts(E), Rpad = padded_ranks(R);
   const int Wc = Epad + Rpad;
   AssignSmem s;
+  // bytes of everything but the count rows (barriers, histograms, scans)
+  const int other = 16 + kLayoutWarps * E * 4 + ((E + 1 + 3) & ~3) * 4 + 2 * Epad * 4 +
+                    ((R + 1 + 3) & ~3) * 4 + 2 * Rpad * 4 + 36 * 4;
   int rows, nbuf;
-  if (num_tiles >= 1 && num_tiles * Wc <= kScanWholeInts) {
+  if (num_tiles >= 1 && other + num_tiles * Wc * 4 <= kAssignSmemBudget) {
     rows = num_tiles;  // the whole matrix in one bulk copy
     nbuf = 1;
   } else {

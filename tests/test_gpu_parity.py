@@ -121,6 +121,10 @@ MEDIUM = {
     "skew_small": workloads.Workload("skew_small", 700, 512, 64, 6, 8, True,
                                      zipf_alpha=1.2, mask_frac=0.05),
     "many_tiles": workloads.Workload("many_tiles", 70000, 8, 256, 8, 8, False),
+    # 2048 experts over 31 tiles: the tile-count matrix exceeds shared
+    # memory and is streamed through the two-buffer ring
+    "ring_scan": workloads.Workload("ring_scan", 1000, 128, 2048, 8, 64, False,
+                                    expert_alignment=4, mask_frac=0.05),
     # more than 64 destination ranks (byte-wise rank rows), both layout paths
     "wide_ranks_small": workloads.Workload("wide_ranks_small", 100, 128, 256, 8, 128, False,
                                            expert_alignment=4, mask_frac=0.05),
