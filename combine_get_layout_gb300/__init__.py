@@ -53,6 +53,7 @@ ABI_SYMBOLS = (
     "ep_combine_to_host",
     "ep_check_error",
     "ep_selftest_wait_timeout",
+    "ep_selftest_fp8_quotient",
     "ep_last_cuda_error",
     "ep_get_layout_noalloc",
     "ep_status_str",
@@ -137,6 +138,8 @@ def _load():
     L.ep_combine_to_host.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, i32, vp]
     L.ep_check_error.restype = i32
     L.ep_check_error.argtypes = [P(EpLayout), vp]
+    L.ep_selftest_fp8_quotient.restype = i32
+    L.ep_selftest_fp8_quotient.argtypes = [vp, vp, vp]
     L.ep_selftest_wait_timeout.restype = i32
     L.ep_selftest_wait_timeout.argtypes = [i64, vp, vp]
     L.ep_get_layout_noalloc.restype = i32
@@ -258,6 +261,10 @@ def ep_combine_to_host(cfg, layout, d_expert_out, d_topk_weights, d_y, h_y, num_
 
 def ep_check_error(layout, stream) -> int:
     return int(_lib.ep_check_error(ctypes.byref(layout), stream))
+
+
+def ep_selftest_fp8_quotient(d_counts, d_first, stream) -> int:
+    return int(_lib.ep_selftest_fp8_quotient(d_counts, d_first, stream))
 
 
 def ep_selftest_wait_timeout(timeout_ns, d_err, stream) -> int:

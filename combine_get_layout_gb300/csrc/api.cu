@@ -685,6 +685,15 @@ int32_t ep_check_error(const ep_layout* layout, void* stream) {
   return status_from_bits(bits);
 }
 
+int32_t ep_selftest_fp8_quotient(uint64_t* d_counts, int32_t* d_first, void* stream) {
+  if (d_counts == nullptr || d_first == nullptr || !aligned16(d_counts))
+    return EP_ERR_INVALID_ARG;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
+  return cuda_status(launch_fp8_quotient_selftest(
+      reinterpret_cast<unsigned long long*>(d_counts), d_first,
+      static_cast<cudaStream_t>(stream)));
+}
+
 int32_t ep_selftest_wait_timeout(int64_t timeout_ns, int32_t* d_err, void* stream) {
   if (d_err == nullptr || !aligned16(d_err)) return EP_ERR_INVALID_ARG;
   if (timeout_ns < 1000 || timeout_ns > 1000000000) return EP_ERR_INVALID_ARG;

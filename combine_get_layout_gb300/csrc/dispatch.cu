@@ -67,6 +67,24 @@ __device__ __forceinline__ int64_t scale_index(int64_t row, int blk, int nblk, i
   return kColMajor ? int64_t(blk) * ld + row : row * nblk + blk;
 }
 
+// x / s for a block scale s >= kFastScaleMin and |x| <= 448 s, given
+// y = RN(1/s): q0 = x * y, then one correction with the exact residual
+// r = x - q0 * s (one FMA), after Markstein's FMA-based division
+// (P. Markstein, "IA-64 and Elementary Functions", 2000).  The reciprocal
+// is taken once per block.  The quotient can differ from the IEEE one in
+// the last fp32 bit, but never in the E4M3 code it rounds to: the inputs
+// here are bf16 values and the scale of a bf16 block maximum, and
+// ep_selftest_fp8_quotient compares the codes against those of the IEEE
+// division over that whole domain (every bf16 maximum, every bf16 value).
+constexpr float kFastScaleMin = 0x1p-100f;
+
+__device__ __forceinline__ float scaled_quotient(float x, float s, float y) {
+  const float q0 = x * y;
+  const float r = fmaf(-q0, s, x);
+  // s > 0: the quotient has x's sign (the correction would turn -0 into +0)
+  return copysignf(fmaf(r, y, q0), x);
+}
+
 // One CTA per token; thread u owns 16 consecutive channels (two 16-byte
 // loads), so 8 lanes cover one 128-channel block: exact amax by three
 // shuffles, scale = amax / 448, 16 E4M3 bytes written with one 16-byte store
@@ -120,9 +138,17 @@ __global__ void __launch_bounds__(1024)
     if (amax != 0.0f) {
       scale = __fdiv_rn(amax, 448.0f);
       uint32_t p[8];
+      if (scale >= kFastScaleMin) {
+        const float y = __frcp_rn(scale);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        p[j] = pack_e4m3x2(__fdiv_rn(f[2 * j], scale), __fdiv_rn(f[2 * j + 1], scale));
+        for (int j = 0; j < 8; ++j)
+          p[j] = pack_e4m3x2(scaled_quotient(f[2 * j], scale, y),
+                             scaled_quotient(f[2 * j + 1], scale, y));
+      } else {  // 1 / scale would overflow: divide
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          p[j] = pack_e4m3x2(__fdiv_rn(f[2 * j], scale), __fdiv_rn(f[2 * j + 1], scale));
+      }
       q.x = p[0] | (p[1] << 16);
       q.y = p[2] | (p[3] << 16);
       q.z = p[4] | (p[5] << 16);
@@ -230,6 +256,58 @@ cudaError_t launch_wait_selftest(uint64_t timeout_ns, int32_t* err, cudaStream_t
 }
 
 cudaError_t prepare_dispatch_kernels() { return cudaSuccess; }
+
+// Exhaustive check of scaled_quotient: block b takes the block maximum
+// amax = the positive finite bf16 with bits b + 1, every thread a share of
+// the 65536 bf16 values x with |x| <= amax; counts[0] += pairs whose E4M3
+// codes differ from those of __fdiv_rn, counts[1] += pairs whose fp32
+// quotients differ, counts[2] += those of them whose IEEE quotient is a
+// normal fp32 number; *first = (amax bits << 16 | x bits) of one code
+// mismatch.
+__global__ void __launch_bounds__(256)
+    fp8_quotient_selftest_kernel(unsigned long long* __restrict__ counts,
+                                 int32_t* __restrict__ first) {
+  const uint32_t ab = blockIdx.x + 1;
+  const float amax = __uint_as_float(ab << 16);
+  const float s = __fdiv_rn(amax, 448.0f);
+  unsigned long long bad_code = 0, bad_f32 = 0, bad_normal = 0;
+  if (s >= kFastScaleMin) {
+    const float y = __frcp_rn(s);
+    for (uint32_t xb = threadIdx.x; xb < 65536u; xb += blockDim.x) {
+      const float x = __uint_as_float(xb << 16);
+      if (!(fabsf(x) <= amax)) continue;  // also NaN
+      const float qa = scaled_quotient(x, s, y), qb = __fdiv_rn(x, s);
+      const bool differ = __float_as_uint(qa) != __float_as_uint(qb);
+      bad_f32 += differ;
+      bad_normal += differ && fabsf(qb) >= 0x1p-126f;
+      if (pack_e4m3x2(qa, 0.0f) != pack_e4m3x2(qb, 0.0f)) {
+        ++bad_code;
+        atomicCAS(first, -1, int32_t((ab << 16) | xb));
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    bad_code += __shfl_xor_sync(0xffffffffu, bad_code, o);
+    bad_f32 += __shfl_xor_sync(0xffffffffu, bad_f32, o);
+    bad_normal += __shfl_xor_sync(0xffffffffu, bad_normal, o);
+  }
+  if ((threadIdx.x & 31) == 0 && (bad_code | bad_f32)) {
+    atomicAdd(&counts[0], bad_code);
+    atomicAdd(&counts[1], bad_f32);
+    atomicAdd(&counts[2], bad_normal);
+  }
+}
+
+cudaError_t launch_fp8_quotient_selftest(unsigned long long* counts, int32_t* first,
+                                         cudaStream_t stream) {
+  cudaError_t st = cudaMemsetAsync(counts, 0, 3 * sizeof(unsigned long long), stream);
+  if (st == cudaSuccess) st = cudaMemsetAsync(first, 0xff, sizeof(int32_t), stream);
+  if (st != cudaSuccess) return st;
+  // positive finite bf16: bits 0x0001 .. 0x7f7f
+  fp8_quotient_selftest_kernel<<<0x7f7f, 256, 0, stream>>>(counts, first);
+  return cudaGetLastError();
+}
 
 static int threads_for(int n) { return n < 1024 ? ((n + 31) / 32) * 32 : 1024; }
 

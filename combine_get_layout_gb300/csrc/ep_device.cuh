@@ -148,13 +148,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // ---- streaming global access ---------------------------------------------
 
-// 16-byte read-only load that does not allocate in L1 (data read once).
 // Row-split kernels: a token's row of 16-byte vectors is shared by
 // gridDim.y CTAs; the CTA's threads start at first_vec() and step by
 // vec_stride().
 __device__ __forceinline__ int first_vec() { return blockIdx.y * blockDim.x + threadIdx.x; }
 __device__ __forceinline__ int vec_stride() { return blockDim.x * gridDim.y; }
 
+// 16-byte read-only load that does not allocate in L1 (data read once).
 __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

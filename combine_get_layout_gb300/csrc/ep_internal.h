@@ -163,6 +163,12 @@ inline void split_row(int nvec, int cap, dim3* block, int* parts) {
 // rows when it sums over destination ranks).
 constexpr int kCombineMaxSlots = 64;
 
+// Exhaustive check of the FP8 dispatch's quotient against the IEEE division
+// (counts[3]: E4M3 code mismatches, fp32 mismatches, fp32 mismatches with
+// a normal IEEE quotient; first: one code mismatch or -1).
+cudaError_t launch_fp8_quotient_selftest(unsigned long long* counts, int32_t* first,
+                                         cudaStream_t stream);
+
 // One CTA waiting (bounded) on a barrier nothing completes.
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, int32_t* err, cudaStream_t stream);
 

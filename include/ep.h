@@ -399,6 +399,24 @@ EP_API int32_t ep_combine_to_host(const ep_config *cfg, const ep_layout *layout,
  * and EP_ERR_TIMEOUT if a bounded on-chip wait of a later call gave up. */
 EP_API int32_t ep_check_error(const ep_layout *layout, void *stream);
 
+/* Self-test of the FP8 dispatch arithmetic ("Deep Dive - DeepEP",
+ * "Precision: FP8 on the wire, BF16 for the reduction": one fp32 scale per
+ * 128 values; the scale here is amax / 448 and each value is quantised from
+ * x / scale rounded to nearest).  The dispatch forms x / scale as a product
+ * with the block's reciprocal plus one fused multiply-add correction, which
+ * may differ from the IEEE quotient in its last bit; this runs it for every
+ * positive finite bf16 block maximum and every bf16 value x with
+ * |x| <= amax (about 2^31 pairs: the whole input domain) beside the IEEE
+ * division and compares the E4M3 codes.
+ * d_counts: device uint64 [3], 16-byte aligned: [0] = pairs whose E4M3
+ * codes differ (0: the dispatch's codes equal those of the IEEE division),
+ * [1] = pairs whose fp32 quotients differ, [2] = those of them whose IEEE
+ * quotient is a normal fp32 number (information only).  d_first: device int32, -1 or (amax bits << 16 | x bits)
+ * of one code mismatch.  Asynchronous on `stream`.  Returns EP_OK or an
+ * error. */
+EP_API int32_t ep_selftest_fp8_quotient(uint64_t *d_counts, int32_t *d_first,
+                                        void *stream);
+
 /* Self-test of the bounded on-chip wait used by the pipelined kernels:
  * launches one CTA that waits on a shared-memory barrier nothing will ever
  * complete, with a limit of timeout_ns nanoseconds.  The wait gives up, the

@@ -157,3 +157,24 @@ def test_fp8_dispatch_argument_checks(ep):
             (wl.num_tokens, wl.hidden // 128), device="cuda"))
     with pytest.raises(ep.EpError):      # scales missing
         ep.dispatch_fp8(cfg, L, x_q=xq)
+
+
+def test_fp8_quotient_exhaustive(ep):
+    """The dispatch's x / scale (reciprocal product plus one FMA correction)
+    gives the E4M3 code of the IEEE division for every bf16 block maximum and
+    every bf16 value in its block (about 2^31 pairs: the whole input domain,
+    so the FP8 payloads equal the oracle's for any input).  The fp32
+    quotients themselves may differ in the last bit; those counts are
+    reported, not asserted."""
+    counts = torch.zeros(4, dtype=torch.int64, device="cuda")
+    first = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = ep.ep_selftest_fp8_quotient(counts.data_ptr(), first.data_ptr(),
+                                     torch.cuda.current_stream().cuda_stream)
+    assert st == ep.EP_OK
+    torch.cuda.synchronize()
+    c = counts.cpu().numpy()
+    f = int(first.item())
+    assert c[0] == 0, (c, hex(f & 0xFFFFFFFF))
+    print(f"fp32 quotients differing (same E4M3 codes): {int(c[1])}, "
+          f"of which with a normal IEEE quotient: {int(c[2])}")
+

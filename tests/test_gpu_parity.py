@@ -343,8 +343,10 @@ def test_dispatch_fp8_bit_exact(ep, name, zp):
 
 
 def test_dispatch_fp8_special_rows(ep):
-    """Zero blocks, saturation-size values, tiny values, signed zeros."""
-    T, H = 8, 512
+    """Zero blocks, saturation-size values, tiny values, signed zeros, and
+    rows whose block scales lie on both sides of 2^-100 (below it the
+    dispatch divides; above it, reciprocal product plus FMA correction)."""
+    T, H = 16, 512
     rng = np.random.default_rng(12)
     xf = rng.standard_normal((T, H)).astype(np.float32)
     xf[0] = 0.0                                 # all-zero row: scale 0, q 0
@@ -354,6 +356,8 @@ def test_dispatch_fp8_special_rows(ep):
     xf[4, ::2] = -0.0
     xf[5, :] = 448.0 * np.sign(xf[5])           # every element at amax
     xf[6, 5] = 3.0e38                           # one block dominated by one value
+    for r, e in zip(range(8, 16), [-90, -95, -99, -100, -101, 60, 100, 120]):
+        xf[r] *= np.float32(2.0 ** e)
     x = workloads.to_bf16_bits(xf)
     idx = np.array([[t % 4, 4 + t % 4] for t in range(T)], np.int64)
     wl = workloads.Workload("fp8s", T, H, 8, 2, 2, True, expert_alignment=4)
