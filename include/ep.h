@@ -27,7 +27,9 @@
  * Conventions for every entry point
  *  - Pointers named d_* or documented "device" are CUDA device pointers; all
  *    buffers are allocated and owned by the CALLER.  The library never
- *    allocates, frees or keeps a pointer after a call returns.
+ *    allocates or frees memory and keeps no pointer after a call returns.
+ *    (The host-buffer entry points create one copy stream and a few events
+ *    per device on first use, kept until exit.)
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Work is enqueued asynchronously on it; a call returns before
  *    the GPU has finished unless documented otherwise.
@@ -124,7 +126,8 @@ typedef struct {
 EP_API int64_t ep_recv_capacity(const ep_config *cfg);
 
 /* Bytes of device scratch memory ep_get_layout needs in layout->workspace
- * (per-tile expert histograms and bases).  Returns -1 if the config is
+ * (per-tile expert and rank counts, per-tile error bits); layouts of at
+ * most 4096 (t, k) pairs do not touch it.  Returns -1 if the config is
  * invalid. */
 EP_API int64_t ep_layout_workspace_bytes(const ep_config *cfg);
 
@@ -137,7 +140,8 @@ EP_API int64_t ep_layout_workspace_bytes(const ep_config *cfg);
  * A rows, and assigns each (t, k) its row: within an expert, rows follow
  * source-global order (source rank, token, k) -- the pages' deterministic
  * mode, produced directly.  Logical source ranks own contiguous token
- * blocks, so that order is (t, k) order.  Runs three kernels on `stream`.
+ * blocks, so that order is (t, k) order.  Runs one kernel on `stream` when
+ * num_tokens * K <= 4096, else two.
  *
  * h_expert_count: NULL for a fully asynchronous call.  If non-NULL (host
  * memory, E int32), the call synchronises `stream`, copies the per-expert
@@ -201,8 +205,8 @@ EP_API int32_t ep_combine(const ep_config *cfg, const ep_layout *layout,
  * layout->workspace is ignored (it may be NULL): the per-tile scratch lives
  * in a 1 MiB array in the library's own device memory, which every GPU that
  * loads the library holds until the process exits.  Configurations whose
- * ep_layout_workspace_bytes exceeds 1 MiB (152 * 4 * (E rounded up to 4,
- * plus R, plus 1) bytes, roughly) are rejected with EP_ERR_CAPACITY before
+ * ep_layout_workspace_bytes exceeds 1 MiB (152 * 4 * (E rounded up to 4 +
+ * R rounded up to 4) + 608 bytes) are rejected with EP_ERR_CAPACITY before
  * anything is launched.  Nothing is allocated or freed, by this call or by
  * any routine it calls.
  *
@@ -411,13 +415,14 @@ EP_API int32_t ep_check_error(const ep_layout *layout, void *stream);
  * d_counts: device uint64 [3], 16-byte aligned: [0] = pairs whose E4M3
  * codes differ (0: the dispatch's codes equal those of the IEEE division),
  * [1] = pairs whose fp32 quotients differ, [2] = those of them whose IEEE
- * quotient is a normal fp32 number (information only).  d_first: device int32, -1 or (amax bits << 16 | x bits)
- * of one code mismatch.  Asynchronous on `stream`.  Returns EP_OK or an
- * error. */
+ * quotient is a normal fp32 number (information only).  d_first: device
+ * int32, -1 or (amax bits << 16 | x bits) of one code mismatch.
+ * Asynchronous on `stream`.  Returns EP_OK or an error. */
 EP_API int32_t ep_selftest_fp8_quotient(uint64_t *d_counts, int32_t *d_first,
                                         void *stream);
 
-/* Self-test of the bounded on-chip wait used by the pipelined kernels:
+/* Self-test of the bounded on-chip wait (the layout kernel's wait for its
+ * bulk copies):
  * launches one CTA that waits on a shared-memory barrier nothing will ever
  * complete, with a limit of timeout_ns nanoseconds.  The wait gives up, the
  * kernel records EP_ERR_TIMEOUT in d_err (device int32, OR-ed in) and
