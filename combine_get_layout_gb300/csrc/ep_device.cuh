@@ -114,38 +114,6 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src,
       : "memory");
 }
 
-// shared -> global, tracked by the issuing thread's bulk async-groups.
-__device__ __forceinline__ void bulk_store(void* gmem_dst, const void* smem_src,
-                                           uint32_t bytes) {
-  asm volatile(
-      "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-          gmem_dst),
-      "r"(smem_addr(smem_src)), "r"(bytes)
-      : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// At most N committed groups may still be READING shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// At most N committed groups may still be in flight at all.
-template <int N>
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy (bulk copy) reads of the same bytes.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---- streaming global access ---------------------------------------------
 
 // Row-split kernels: a token's row of 16-byte vectors is shared by
