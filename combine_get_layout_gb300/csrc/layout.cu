@@ -615,59 +615,51 @@ __global__ void __launch_bounds__(kLayoutThreads)
   pdl_wait();
   pdl_launch_dependents();
 
-  // The whole input, range-checked (an id outside [-1, E) is reported and
-  // read as -1), in shared memory: one pass of independent loads.
-  int errbits = 0;
-#pragma unroll 4
-  for (int i = tid; i < T * K; i += blockDim.x) s_idx[i] = read_expert(topk_idx + i, E, errbits);
-  __syncthreads();
-
   // This CTA's tokens [ctb, cte).
   const int tt = (T + gridDim.x - 1) / gridDim.x;
   const int ctb = min(T, int(blockIdx.x) * tt), cte = min(T, ctb + tt);
   const int Eg = E / R;
 
-  // Survey, one token per thread: repeat checks, the token's destination
-  // ranks (counted once each), expert counts per region (warp-aggregated:
-  // lanes with the same expert and region add once).
-  for (int t0 = 0; t0 < T; t0 += blockDim.x) {
-    const int t = t0 + tid;
-    const bool live = t < T;
-    const int region = t < ctb ? 0 : (t < cte ? 1 : 2);
-    int32_t* h = hist + region * Epad;
-    int32_t* rc = rcnt + region * Rpad;
-    uint64_t mask = 0;
-    if (live && region == 1 && R > 64)   // wide rows: cleared, then set per rank
-      for (int r = 0; r < R; ++r) is_token_in_rank[int64_t(t) * R + r] = 0;
-    const int32_t* row = s_idx + t * K;
-    for (int k = 0; k < K; ++k) {
-      const int e = live ? row[k] : -1;
-      if (e >= 0) {
-        for (int j = 0; j < k; ++j)
-          if (row[j] == e) errbits |= ERRBIT_DUP_EXPERT;
+  // The whole input, range-checked (an id outside [-1, E) is reported and
+  // read as -1), in shared memory: one pass of independent loads.  The rank
+  // rows of this CTA's tokens are cleared meanwhile (set per rank below).
+  int errbits = 0;
+#pragma unroll 4
+  for (int i = tid; i < T * K; i += blockDim.x) s_idx[i] = read_expert(topk_idx + i, E, errbits);
+  for (int i = tid; i < (cte - ctb) * R; i += blockDim.x)
+    is_token_in_rank[int64_t(ctb) * R + i] = 0;
+  __syncthreads();
+
+  // Survey in token-aligned warp steps: lanes [0, TPS*K) hold the pairs of
+  // TPS consecutive tokens.  Each lane adds its pair to its region's expert
+  // count, and looks at the earlier selections of its own token (a
+  // broadcast read of one shared row): the same expert again is a repeat;
+  // no earlier expert on the same rank makes it the token's first on that
+  // rank, which adds one to the region's rank count and, for this CTA's own
+  // tokens, sets the rank-row flag.
+  {
+    const int TPS = 32 / K, SP = TPS * K;
+    const int steps = (T + TPS - 1) / TPS;
+    const int tl = lane / K, kk = lane - tl * K;
+    for (int st = warp; st < steps; st += kLayoutWarps) {
+      const int t = st * TPS + tl;
+      const bool live = lane < SP && t < T;
+      const int32_t* row = s_idx + (st * SP + tl * K);
+      const int e = live ? row[kk] : -1;
+      if (e < 0) continue;
+      const int region = t < ctb ? 0 : (t < cte ? 1 : 2);
+      atomicAdd(&hist[region * Epad + e], 1);
+      const int r = e / Eg, lo = r * Eg, hi = lo + Eg;
+      bool first = true;
+      for (int j = 0; j < kk; ++j) {
+        const int ej = row[j];
+        if (ej == e) errbits |= ERRBIT_DUP_EXPERT;
+        if (ej >= lo && ej < hi) first = false;
       }
-      const int key = e >= 0 ? e * 3 + region : -1 - lane;
-      const uint32_t peers = __match_any_sync(0xffffffffu, key);
-      if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&h[e], __popc(peers));
-      if (e >= 0) {
-        const int r = e / Eg;
-        if (R <= 64) {
-          mask |= uint64_t(1) << r;
-        } else {
-          // a rank counted at its first selection in k order
-          bool first = true;
-          for (int j = 0; j < k; ++j)
-            if (row[j] >= 0 && row[j] / Eg == r) first = false;
-          if (first) {
-            atomicAdd(&rc[r], 1);
-            if (region == 1) is_token_in_rank[int64_t(t) * R + r] = 1;
-          }
-        }
+      if (first) {
+        atomicAdd(&rcnt[region * Rpad + r], 1);
+        if (region == 1) is_token_in_rank[int64_t(t) * R + r] = 1;
       }
-    }
-    if (live && R <= 64) {
-      for (uint64_t m = mask; m; m &= m - 1) atomicAdd(&rc[__ffsll(m) - 1], 1);
-      if (region == 1) write_rank_row(is_token_in_rank + int64_t(t) * R, R, mask);
     }
   }
   if (errbits) atomicOr(&s_scr[33], errbits);
