@@ -8,8 +8,9 @@
 // surveys the whole input (layout_small_kernel below).  Otherwise two
 // launches, no inter-CTA waiting:
 //   1. count  (one CTA per token tile): validate topk_idx, per-tile expert
-//      histogram with warp-aggregated shared-memory atomics, per-rank dedup
-//      flags and per-tile rank counts.
+//      histogram with shared-memory adds, per-rank dedup flags (a token's
+//      selections compared across lanes by shuffles) and per-tile rank
+//      counts.
 //   2. assign (one CTA per tile, plus CTAs for padding when there are few
 //      tiles): every CTA streams the whole tile-count matrix into shared
 //      memory with bulk copies (TMA) and scans it itself -- its own tile
@@ -96,54 +97,51 @@ constexpr int kSurveyUnroll = 4;
 
 // One warp step over the selections of whole tokens: lanes [0, TPS*K) hold
 // the pairs [base, base + TPS*K) of the tile (lanes past `pe` or past the
-// step hold e = -1).  Counts experts into `hist` (leader lanes only; atomics
-// when several warps share it), flags an expert repeated within a token, and
-// writes the tokens' destination-rank rows (unless itr_tile is null) and
-// per-rank token counts.  `sr` is this warp's 32-int shared scratch.  All
-// lanes call.
-template <bool kSharedHist>
+// step hold e = -1), so a token's K selections sit in adjacent lanes.  Each
+// lane adds its pair to `hist` and reads its token's selections by
+// shuffles: the same expert at an earlier k is a repeat; no earlier
+// selection on the same rank makes it the token's first on that rank, which
+// adds one to s_rank; the token's first lane writes the token's
+// destination-rank row.  All lanes call.
 __device__ __forceinline__ void survey_step(int e, int lane, int base, int pe, int K,
                                             int TPS, int Eg, int R, int32_t* hist,
-                                            int32_t* sr, uint8_t* itr_tile,
-                                            int32_t* s_rank, int& errbits) {
-  uint32_t peers = __match_any_sync(0xffffffffu, e);
-  if (e >= 0 && lane == __ffs(peers) - 1) {
-    if (kSharedHist) atomicAdd(&hist[e], __popc(peers));
-    else hist[e] += __popc(peers);
-  }
-  // the same expert twice in one token: equal (expert, token-in-step) keys
-  const int key = e >= 0 ? ((e << 5) | (lane / K)) : -1 - lane;
-  const uint32_t same = __match_any_sync(0xffffffffu, key);  // all lanes execute it
-  if (e >= 0 && __popc(same) > 1) errbits |= ERRBIT_DUP_EXPERT;
-  sr[lane] = e >= 0 ? e / Eg : -1;
-  __syncwarp();
-  if (lane < TPS && base + lane * K < pe) {
-    const int32_t* mine = sr + lane * K;
-    const int tl = base / K + lane;  // token index within the tile
-    if (R <= 64) {
-      uint64_t mask = 0;
-      for (int k = 0; k < K; ++k)
-        if (mine[k] >= 0) mask |= uint64_t(1) << mine[k];
-      if (itr_tile != nullptr) write_rank_row(itr_tile + int64_t(tl) * R, R, mask);
-      for (uint64_t m = mask; m; m &= m - 1) atomicAdd(&s_rank[__ffsll(m) - 1], 1);
-    } else {
-      for (int r = 0; r < R; ++r) {
-        int in = 0;
-        for (int k = 0; k < K; ++k) in |= mine[k] == r;
-        if (itr_tile != nullptr) itr_tile[int64_t(tl) * R + r] = static_cast<uint8_t>(in);
-        if (in) atomicAdd(&s_rank[r], 1);
-      }
+                                            uint8_t* itr_tile, int32_t* s_rank,
+                                            int& errbits) {
+  const int tl = lane / K, kk = lane - tl * K, g0 = tl * K;
+  const bool token_live = lane < TPS * K && base + g0 < pe;
+  if (e >= 0) atomicAdd(&hist[e], 1);
+  const int r = e >= 0 ? e / Eg : -1;
+  bool first = true;
+  uint64_t mask = 0;
+  for (int j = 0; j < K; ++j) {
+    // lanes past the step read wrapped lanes; their results are unused
+    const int ej = __shfl_sync(0xffffffffu, e, (g0 + j) & 31);
+    const int rj = __shfl_sync(0xffffffffu, r, (g0 + j) & 31);
+    if (ej < 0) continue;
+    if (R <= 64) mask |= uint64_t(1) << rj;
+    if (j < kk) {
+      if (ej == e) errbits |= ERRBIT_DUP_EXPERT;
+      if (rj == r) first = false;
     }
   }
+  const bool lead = token_live && kk == 0;
+  uint8_t* row = itr_tile + int64_t(base / K + tl) * R;
+  if (R <= 64) {
+    if (lead) write_rank_row(row, R, mask);
+  } else {
+    if (lead)
+      for (int q = 0; q < R; ++q) row[q] = 0;
+    __syncwarp();
+    if (e >= 0 && first) row[r] = 1;
+  }
+  if (e >= 0 && first) atomicAdd(&s_rank[r], 1);
   __syncwarp();
 }
 
 // A warp's whole survey of its token-aligned span [tb, te) of a tile.
-template <bool kSharedHist>
 __device__ __forceinline__ void survey_span(const int64_t* __restrict__ src, int tb, int te,
                                             int K, int E, int R, int lane, int32_t* hist,
-                                            int32_t* sr, uint8_t* itr_tile,
-                                            int32_t* s_rank, int& errbits) {
+                                            uint8_t* itr_tile, int32_t* s_rank, int& errbits) {
   const int TPS = 32 / K, SP = TPS * K, Eg = E / R;
   const int pb = tb * K, pe = te * K;
   for (int b0 = pb; b0 < pe; b0 += SP * kSurveyUnroll) {
@@ -157,8 +155,7 @@ __device__ __forceinline__ void survey_span(const int64_t* __restrict__ src, int
     for (int u = 0; u < kSurveyUnroll; ++u) {
       const int base = b0 + u * SP;
       if (base >= pe) break;
-      survey_step<kSharedHist>(ev[u], lane, base, pe, K, TPS, Eg, R, hist, sr, itr_tile,
-                               s_rank, errbits);
+      survey_step(ev[u], lane, base, pe, K, TPS, Eg, R, hist, itr_tile, s_rank, errbits);
     }
   }
 }
@@ -177,7 +174,6 @@ __global__ void __launch_bounds__(kLayoutThreads)
   const int Wc = count_row_width(E, R);
   int32_t* hist = smem_i32;                  // [Wc]: experts, then ranks
   int32_t* rcnt = hist + padded_experts(E);  // [Rpad]
-  int32_t* wscr = hist + Wc;                 // [kLayoutWarps * 32]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   if (tid == 0) s_err = 0;
@@ -191,12 +187,12 @@ __global__ void __launch_bounds__(kLayoutThreads)
   const int nt = min(tile_tokens, T - t0);
   const int64_t* src = topk_idx + int64_t(t0) * K;
   int err = 0;
-  // Warps take token-aligned spans: expert histogram (warp-aggregated
-  // shared atomics), duplicate experts, destination ranks.
+  // Warps take token-aligned spans: expert histogram (shared adds),
+  // duplicate experts, destination ranks.
   const int span = (nt + kLayoutWarps - 1) / kLayoutWarps;
   const int tb = min(nt, warp * span), te = min(nt, tb + span);
-  survey_span<true>(src, tb, te, K, E, R, lane, hist, wscr + warp * 32,
-                    is_token_in_rank + int64_t(t0) * R, rcnt, err);
+  survey_span(src, tb, te, K, E, R, lane, hist, is_token_in_rank + int64_t(t0) * R, rcnt,
+              err);
   if (err) atomicOr(&s_err, err);
   __syncthreads();
 
@@ -368,11 +364,8 @@ __global__ void __launch_bounds__(kLayoutThreads)
       ev[u] = p < pe ? read_expert(src + p, E, ignored) : -1;
     }
 #pragma unroll
-    for (int u = 0; u < kSurveyUnroll; ++u) {
-      if (b0 + u * 32 >= pe) break;
-      const uint32_t peers = __match_any_sync(0xffffffffu, ev[u]);
-      if (ev[u] >= 0 && lane == __ffs(peers) - 1) my[ev[u]] += __popc(peers);
-    }
+    for (int u = 0; u < kSurveyUnroll; ++u)
+      if (ev[u] >= 0) atomicAdd(&my[ev[u]], 1);
   }
 
   // Per expert: rows of earlier tiles (this tile's base) and of all tiles.
@@ -765,7 +758,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
 
 static int count_smem(int E, int R, int K) {
   (void)K;
-  return (count_row_width(E, R) + kLayoutWarps * 32) * 4;
+  return count_row_width(E, R) * 4;
 }
 
 cudaError_t prepare_layout_kernels() {
