@@ -236,8 +236,9 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int32_t* s_warp,
 
 struct AssignSmem {
   // byte offsets into dynamic shared memory
-  int bar, ring, whist, start, base, total, rstart, rbase, rtotal, scratch, bytes;
+  int bar, ring, whist, start, base, total, rstart, rbase, rtotal, scratch, part, bytes;
   int chunk_rows;
+  int row_groups;   // row groups of the column sums (see sum_columns)
 };
 
 // Shared-memory plan of the assign kernel; identical on host and device.
@@ -245,9 +246,14 @@ __host__ __device__ inline AssignSmem assign_smem(int E, int R, int num_tiles) {
   const int Epad = padded_experts(E), Rpad = padded_ranks(R);
   const int Wc = Epad + Rpad;
   AssignSmem s;
-  // bytes of everything but the count rows (barriers, histograms, scans)
+  // column sums: 4 columns a thread; the threads left over take row groups
+  const int col_groups = Wc / 4;
+  s.row_groups = col_groups < kLayoutThreads ? kLayoutThreads / col_groups : 1;
+  const int part_bytes = 2 * s.row_groups * Wc * 4;
+  // bytes of everything but the count rows (barriers, histograms, scans,
+  // partial sums)
   const int other = 16 + kLayoutWarps * E * 4 + ((E + 1 + 3) & ~3) * 4 + 2 * Epad * 4 +
-                    ((R + 1 + 3) & ~3) * 4 + 2 * Rpad * 4 + 36 * 4;
+                    ((R + 1 + 3) & ~3) * 4 + 2 * Rpad * 4 + 36 * 4 + part_bytes;
   int rows, nbuf;
   if (num_tiles >= 1 && other + num_tiles * Wc * 4 <= kAssignSmemBudget) {
     rows = num_tiles;  // the whole matrix in one bulk copy
@@ -269,7 +275,8 @@ __host__ __device__ inline AssignSmem assign_smem(int E, int R, int num_tiles) {
   s.rbase = s.rstart + ((R + 1 + 3) & ~3) * 4; // R
   s.rtotal = s.rbase + Rpad * 4;               // R
   s.scratch = s.rtotal + Rpad * 4;             // 32 + 4
-  s.bytes = s.scratch + 36 * 4;
+  s.part = s.scratch + 36 * 4;                 // 2 x row_groups x Wc
+  s.bytes = s.part + part_bytes;
   return s;
 }
 
@@ -304,6 +311,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
   int32_t* s_rbase = reinterpret_cast<int32_t*>(smem + L.rbase);
   int32_t* s_rtotal = reinterpret_cast<int32_t*>(smem + L.rtotal);
   int32_t* s_scr = reinterpret_cast<int32_t*>(smem + L.scratch);
+  int32_t* s_part = reinterpret_cast<int32_t*>(smem + L.part);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x;
   const bool has_tile = tile < num_tiles;
@@ -380,25 +388,46 @@ __global__ void __launch_bounds__(kLayoutThreads)
     const int r0 = ch * rows;
     const int n = min(rows, num_tiles - r0);
     const int32_t* buf = ring + (ch & 1) * rows * Wc;
-    for (int e = tid; e < E; e += blockDim.x) {
-      int b = 0, tot = 0;
-      for (int r = 0; r < n; ++r) {
-        const int v = buf[r * Wc + e];
-        tot += v;
-        b += (r0 + r < tile) ? v : 0;
+    // Column sums -- all rows (totals) and rows of earlier tiles (this
+    // tile's base) -- 4 columns a thread with one 16-byte load a row, rows
+    // split into L.row_groups groups so that many loads are in flight; the
+    // groups' partial sums then meet in shared memory.
+    {
+      const int nb = min(n, max(0, tile - r0));   // rows of earlier tiles
+      const int col_groups = Wc / 4, G = L.row_groups;
+      const int per = (n + G - 1) / G;
+      for (int w = tid; w < col_groups * G; w += blockDim.x) {
+        const int cgi = w % col_groups, g = w / col_groups;
+        const int ra = g * per, rb = min(n, ra + per);
+        int4 tot = make_int4(0, 0, 0, 0), bas = tot;
+#pragma unroll 4
+        for (int r = ra; r < rb; ++r) {
+          const int4 v = *reinterpret_cast<const int4*>(buf + r * Wc + cgi * 4);
+          tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
+          if (r < nb) {
+            bas.x += v.x; bas.y += v.y; bas.z += v.z; bas.w += v.w;
+          }
+        }
+        *reinterpret_cast<int4*>(s_part + (g * Wc + cgi * 4)) = tot;
+        *reinterpret_cast<int4*>(s_part + ((G + g) * Wc + cgi * 4)) = bas;
       }
-      s_base[e] += b;
-      s_total[e] += tot;
-    }
-    for (int q = tid; q < R; q += blockDim.x) {  // rank columns
-      int b = 0, tot = 0;
-      for (int r = 0; r < n; ++r) {
-        const int v = buf[r * Wc + Epad + q];
-        tot += v;
-        b += (r0 + r < tile) ? v : 0;
+      __syncthreads();
+      for (int c = tid; c < Wc; c += blockDim.x) {
+        const bool is_e = c < E, is_r = c >= Epad && c - Epad < R;
+        if (!is_e && !is_r) continue;
+        int tot = 0, bas = 0;
+        for (int g = 0; g < G; ++g) {
+          tot += s_part[g * Wc + c];
+          bas += s_part[(G + g) * Wc + c];
+        }
+        if (is_e) {
+          s_base[c] += bas;
+          s_total[c] += tot;
+        } else {
+          s_rbase[c - Epad] += bas;
+          s_rtotal[c - Epad] += tot;
+        }
       }
-      s_rbase[q] += b;
-      s_rtotal[q] += tot;
     }
     __syncthreads();
     if (tid == 0 && ch + 2 < nchunks) issue(ch + 2);
