@@ -456,3 +456,56 @@ def test_identity_experts_round_trip(ep, name):
     xi = x.view(torch.int16)
     want = torch.where(xi == -32768, torch.zeros_like(xi), xi)
     assert torch.equal(y.view(torch.int16), want)
+
+
+# --------------------------------------------------------------------------
+# extreme configurations: largest hidden size, one expert, every expert
+# selected, largest alignment, one token -- the whole path against the oracle
+# --------------------------------------------------------------------------
+
+EXTREME = {
+    "h_max_bf16": workloads.Workload("h_max_bf16", 24, 49152, 8, 2, 2, False,
+                                     expert_alignment=4),
+    "h_max_fp8": workloads.Workload("h_max_fp8", 24, 49152, 8, 2, 2, True,
+                                    expert_alignment=4),
+    "one_expert": workloads.Workload("one_expert", 100, 256, 1, 1, 1, False,
+                                     expert_alignment=1),
+    "k_eq_e": workloads.Workload("k_eq_e", 64, 256, 32, 32, 4, False, expert_alignment=16),
+    "align_max": workloads.Workload("align_max", 300, 128, 16, 4, 4, True,
+                                    expert_alignment=1024, mask_frac=0.1),
+    "one_token_bf16": workloads.Workload("one_token_bf16", 1, 7168, 256, 8, 8, False),
+    "one_token_fp8": workloads.Workload("one_token_fp8", 1, 7168, 256, 8, 8, True),
+}
+
+
+@pytest.mark.parametrize("name", list(EXTREME))
+@pytest.mark.parametrize("zp", [False, True])
+def test_extreme_configs_whole_path(ep, name, zp):
+    wl = EXTREME[name]
+    inp = workloads.make_inputs(wl, seed=3)
+    cfg = cfg_of(ep, wl, zero_padding=zp)
+    L = run_layout(ep, cfg, inp["topk_idx"])
+    ora = oracle_layout(wl, inp["topk_idx"], cfg.capacity)
+    assert_layout_equal(L, ora, wl.num_tokens)
+    w = dev(inp["topk_weights"])
+    recv, recv_s, recv_w = ep.dispatch(cfg, L, dev_bf16(inp["x"]), w)
+    Y = _expert_out(cfg, 2)
+    y = ep.combine(cfg, L, Y, w)
+    torch.cuda.synchronize()
+    used = int(ora["expert_start"][-1])
+    rows = np.arange(used) if zp else np.nonzero(ora["src_info"][:used, 0] >= 0)[0]
+    if wl.use_fp8_dispatch:
+        ref_q, ref_s, ref_w = oracle.dispatch_fp8(inp["x"], inp["topk_weights"], ora,
+                                                  zero_padding=zp)
+        assert np.array_equal(recv.cpu().numpy()[rows], ref_q[rows])
+        assert np.array_equal(recv_s.cpu().numpy()[rows].view(np.uint32),
+                              ref_s[rows].view(np.uint32))
+    else:
+        ref_x, ref_w = oracle.dispatch_bf16(inp["x"], inp["topk_weights"], ora,
+                                            zero_padding=zp)
+        assert np.array_equal(host_u16(recv)[rows], ref_x[rows])
+    assert np.array_equal(recv_w.cpu().numpy()[rows].view(np.uint32),
+                          ref_w[rows].view(np.uint32))
+    ref_y = oracle.combine(host_u16(Y), inp["topk_weights"], ora["slot_of"])
+    assert np.array_equal(host_u16(y), ref_y)
+
