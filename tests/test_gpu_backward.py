@@ -52,6 +52,8 @@ CASES = {
     "k12": workloads.Workload("k12", 300, 512, 48, 12, 6, False, expert_alignment=8,
                               mask_frac=0.1),
     "decode": workloads.WORKLOADS["decode"].with_(use_fp8_dispatch=False),
+    "k1": workloads.Workload("k1", 257, 256, 16, 1, 16, False, expert_alignment=1),
+    "k_eq_e": workloads.Workload("k_eq_e", 64, 256, 32, 32, 4, False, expert_alignment=16),
     "prefill": workloads.WORKLOADS["prefill"],
 }
 
@@ -74,7 +76,7 @@ def _tokens(wl):
     return np.unique(np.concatenate([[0, wl.num_tokens - 1], rng.choice(wl.num_tokens, 256)]))
 
 
-@pytest.mark.parametrize("name", ["ragged", "k12", "decode"])
+@pytest.mark.parametrize("name", ["ragged", "k12", "decode", "k1", "k_eq_e"])
 def test_dispatch_backward_bit_exact(ep, name):
     wl = CASES[name]
     inp, cfg, L, ora = _setup(ep, wl)

@@ -47,6 +47,11 @@ CASES = {
     "prefill": workloads.WORKLOADS["prefill"],
     "skew": workloads.WORKLOADS["skew"].with_(use_fp8_dispatch=False),
     "many_tiles": workloads.Workload("many_tiles", 70000, 8, 256, 8, 8, False),
+    # one rank owns every expert; one expert per rank
+    "one_rank": workloads.Workload("one_rank", 300, 256, 16, 4, 1, False, expert_alignment=4,
+                                   mask_frac=0.05),
+    "rank_per_expert": workloads.Workload("rank_per_expert", 200, 256, 16, 4, 16, False,
+                                          expert_alignment=4),
 }
 
 
@@ -93,7 +98,8 @@ def test_rank_rows_through_noalloc_entry_point(ep):
     assert np.array_equal(L.rank_src.cpu().numpy()[: rl["rows"]], rl["rank_src"][: rl["rows"]])
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "r64", "r64_small", "skew"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "r64", "r64_small", "skew", "one_rank",
+                                  "rank_per_expert"])
 def test_dispatch_ranks_and_expand(ep, name):
     wl = CASES[name]
     inp, cfg, L, idx, ora, rl = _setup(ep, wl, zp=True)
@@ -120,7 +126,8 @@ def test_dispatch_ranks_and_expand(ep, name):
     assert torch.equal(recv[:used].view(torch.int16), direct[:used].view(torch.int16))
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "r64", "r64_small", "skew", "prefill"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "r64", "r64_small", "skew", "prefill",
+                                  "one_rank", "rank_per_expert"])
 @pytest.mark.parametrize("weighted", [True, False])
 def test_reduce_and_combine_ranks(ep, name, weighted):
     wl = CASES[name]
