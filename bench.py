@@ -2,7 +2,8 @@
 """Benchmark of the MoE dispatch / combine layout path on GB300.
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-layout (2 kernels) -> dispatch -> combine, through the library's C ABI.
+layout (one or two kernels) -> dispatch -> combine, through the library's
+C ABI (with --fused, layout and dispatch in one call).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload prefill]
   python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
@@ -11,11 +12,13 @@ Prints ONE JSON line on rank 0.  Everything else goes to stderr.
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
 and torch.cuda.synchronize() on both sides.  Each step is timed on the
-launching stream with CUDA events (one pair per kernel group), and the L2 is
-flushed before every step, outside the events: a 256 MiB write evicts the
-workload's lines, then a 256 MiB read evicts the write's dirty lines, so that
-no step pays for write-backs of the flush itself; the reported
-ms_per_step is the mean step time, maximum over ranks.  With N > 1 (torchrun)
+launching stream with one pair of CUDA events around the whole step, and the
+L2 is flushed before every step, outside the events: a 256 MiB write evicts
+the workload's lines, then a 256 MiB read evicts the write's dirty lines, so
+that no step pays for write-backs of the flush itself; the reported
+ms_per_step is the mean step time, maximum over ranks.  A second pass of K
+steps with an event between stages gives the per-stage times and the
+roofline's kernel time.  With N > 1 (torchrun)
 every rank runs an independent replica of the workload (weak scaling; the
 path has no cross-rank step on a single-GPU-per-problem layout).
 """
@@ -45,6 +48,8 @@ L2_FLUSH_BYTES = 256 << 20  # twice the GB300's L2
 # (t, k) pairs up to which the layout is one launch (kSmallLayoutPairs in
 # combine_get_layout_gb300/csrc/ep_internal.h); used to count launches
 SMALL_LAYOUT_PAIRS = 4096
+SMALL_LAYOUT_CTAS = 152     # its CTAs (kSmallLayoutCtas)
+SMALL_OWN_PAIRS = 64        # pairs a CTA may own to dispatch them (kSmallOwnPairs)
 
 
 def log(*a):
@@ -81,6 +86,9 @@ def parse_args():
     p.add_argument("--e2e-chunks", type=int, default=8,
                    help="token chunks of the host-buffer entry points in the e2e leg "
                         "(copies of later chunks overlap the kernels of earlier ones)")
+    p.add_argument("--fused", action="store_true",
+                   help="forward pass: layout and dispatch through ep_layout_and_dispatch "
+                        "(one kernel for small inputs)")
     p.add_argument("--graph", action="store_true",
                    help="replay each kernel group from a captured CUDA graph "
                         "(removes host launch overhead; for latency-bound sizes)")
@@ -128,8 +136,17 @@ KERNEL_SOURCES = {
 
 
 def source_sha(kernel: str) -> str:
+    """First 16 hex digits of the SHA-256 of the kernel's .cu file followed by
+    the shared headers it includes (csrc/*.cuh, csrc/*.h, in name order)."""
+    h = hashlib.sha256()
     with open(os.path.join(ROOT, KERNEL_SOURCES[kernel]), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+        h.update(f.read())
+    csrc = os.path.join(ROOT, "combine_get_layout_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel: str, workload: str):
@@ -137,6 +154,8 @@ def profiled_traffic(kernel: str, workload: str):
     kernel's source is unchanged since (source hash recorded beside it)."""
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
+        return None
+    if kernel not in KERNEL_SOURCES:
         return None
     want = source_sha(kernel)
     pat = re.compile(r"TRAFFIC kernel=(\S+) workload=(\S+) bytes_per_launch=(\d+) "
@@ -491,6 +510,9 @@ def run_ours(args):
     # one kernel for at most SMALL_LAYOUT_PAIRS (t, k) pairs, else count +
     # assign.
     lay_launches = 1 if T * K <= SMALL_LAYOUT_PAIRS else 2
+    # one kernel for layout and dispatch (see ep_layout_and_dispatch)
+    fused_small = (0 < T * K <= SMALL_LAYOUT_PAIRS
+                   and -(-T // SMALL_LAYOUT_CTAS) * K <= SMALL_OWN_PAIRS)
     one = 1 if T > 0 else 0
     zp_extra = 1 if args.zero_padding else 0
     backward = args.pass_ == "backward"
@@ -547,6 +569,18 @@ def run_ours(args):
                   ("expand", expand, one + zp_extra),
                   ("reduce_ranks", reduce_ranks, one),
                   ("combine_ranks", combine_ranks, one)]
+    elif args.fused:
+        if fp8_opts:
+            raise SystemExit("--fused takes no FP8 scale-layout or pre-quantised options")
+
+        def layout_dispatch():
+            st = ep.ep_layout_and_dispatch(ccfg, T, p(idx_d), L.c, p(x_d), p(w_d), p(recv_x),
+                                           p(recv_s), p(recv_w), fn_stream[0])
+            assert st == 0, ep.ep_status_str(st)
+
+        stages = [("layout_dispatch", layout_dispatch,
+                   (1 if fused_small else lay_launches + one) + zp_extra),
+                  ("combine", lambda: combine(Y_d, y_d), one)]
     else:
         stages = [("layout", layout, lay_launches),
                   ("dispatch", lambda: dispatch(x_d), one + zp_extra),
@@ -585,11 +619,25 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert ep.ep_check_error(L.c, sptr) == 0
     ns = len(runners)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)]
-          for _ in range(args.steps)]
+    # The timed steps carry events only around the whole step, so that the
+    # library's kernels chain from stage to stage as a caller's would.
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+           for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    for i in range(args.steps):
+        l2_flush()
+        sev[i][0].record(stream)
+        for fn in runners:
+            fn()
+        sev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    # Stage times from a second pass with an event between stages (an event
+    # there breaks the chaining, so its stages add up to more than a step).
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)]
+          for _ in range(args.steps)]
     for i in range(args.steps):
         l2_flush()
         e = ev[i]
@@ -604,7 +652,7 @@ def run_ours(args):
     clocks = sampler.summary(t0, t1)
     stage_ms = {name: [e[j].elapsed_time(e[j + 1]) for e in ev]
                 for j, (name, _, _) in enumerate(stages)}
-    step_ms = [e[0].elapsed_time(e[ns]) for e in ev]
+    step_ms = [a.elapsed_time(b_) for a, b_ in sev]
     ms_local = statistics.mean(step_ms)
     value, ms = job_throughput(T, ms_local, world, device)
 
@@ -627,6 +675,10 @@ def run_ours(args):
                               wl.use_fp8_dispatch and args.fp8_prequant)
         kernels = {"dispatch": "dispatch_fp8_kernel" if wl.use_fp8_dispatch
                    else "dispatch_bf16_kernel", "combine": "combine_kernel"}
+        if args.fused:
+            b["layout_dispatch"] = b["dispatch"]
+            kernels["layout_dispatch"] = ("layout_small_kernel" if fused_small
+                                          else kernels["dispatch"])
     streaming = [name for name, _, _ in stages if name != "layout"]
     avg = {n: statistics.mean(stage_ms[n]) for n in streaming}
     med = {n: statistics.median(stage_ms[n]) for n in streaming}
@@ -643,7 +695,8 @@ def run_ours(args):
                 else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": b[dom]}
     stream_ms = sum(avg.values())
-    breakdown = {"layout_us": 1e3 * statistics.mean(stage_ms["layout"])}
+    breakdown = {"layout_us": (1e3 * statistics.mean(stage_ms["layout"]) if "layout" in stage_ms
+                               else None)}
     for n in streaming:
         breakdown.update({f"{n}_us": 1e3 * avg[n], f"{n}_median_us": 1e3 * med[n],
                           f"{n}_gbs": gbs[n], f"{n}_pct_of_8tbs": 100 * gbs[n] / NOMINAL_HBM_GBS,
@@ -740,6 +793,8 @@ def run_ours(args):
             "dtype": "bf16", "data": "synthetic (seeded router simulation, PCG64; no dataset)",
             "config": workload_config(wl, extra={
                 "l2": "flushed before every step (256 MiB write, then 256 MiB read), outside the step events",
+                "timing": ("step: events around each whole step; stage times and the roofline "
+                           "from a second pass of the same steps with events between stages"),
                 "step": " + ".join(name for name, _, _ in stages) +
                         ("; seeded N(0,1) dy and expert rows" if backward else
                          "; combine reads a device-resident seeded N(0,1) expert-output buffer"),
@@ -750,7 +805,9 @@ def run_ours(args):
                 "combine_bias_tensors": args.bias,
                 "combine_returns_weights": bool(args.return_weights),
                 "fp8_scales": (args.fp8_scales if wl.use_fp8_dispatch else None),
-                "fp8_prequantised_input": bool(wl.use_fp8_dispatch and args.fp8_prequant)}),
+                "fp8_prequantised_input": bool(wl.use_fp8_dispatch and args.fp8_prequant),
+                "layout_and_dispatch": ("one call, one kernel" if args.fused and fused_small
+                                        else "one call" if args.fused else "separate calls")}),
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,

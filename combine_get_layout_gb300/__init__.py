@@ -39,6 +39,7 @@ ABI_SYMBOLS = (
     "ep_get_layout",
     "ep_dispatch",
     "ep_combine",
+    "ep_layout_and_dispatch",
     "ep_scale_ld",
     "ep_dispatch_fp8",
     "ep_combine_epilogue",
@@ -131,6 +132,9 @@ def _load():
     L.ep_reduce_ranks.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp]
     L.ep_combine_ranks.restype = i32
     L.ep_combine_ranks.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp]
+    L.ep_layout_and_dispatch.restype = i32
+    L.ep_layout_and_dispatch.argtypes = [P(EpConfig), i32, vp, P(EpLayout), vp, vp, vp, vp,
+                                         vp, vp]
     L.ep_dispatch_from_host.restype = i32
     L.ep_dispatch_from_host.argtypes = [P(EpConfig), P(EpLayout), vp, vp, vp, vp, vp, vp,
                                         i32, vp]
@@ -244,6 +248,13 @@ def ep_reduce_ranks(cfg, layout, d_topk_idx, d_expert_out, d_topk_weights, d_ran
 def ep_combine_ranks(cfg, layout, d_rank_y, d_y, stream) -> int:
     return int(_lib.ep_combine_ranks(ctypes.byref(cfg), ctypes.byref(layout), d_rank_y,
                                      d_y, stream))
+
+
+def ep_layout_and_dispatch(cfg, num_tokens, d_topk_idx, layout, d_x, d_topk_weights,
+                           d_recv_x, d_recv_scale, d_recv_w, stream) -> int:
+    return int(_lib.ep_layout_and_dispatch(ctypes.byref(cfg), int(num_tokens), d_topk_idx,
+                                           ctypes.byref(layout), d_x, d_topk_weights, d_recv_x,
+                                           d_recv_scale, d_recv_w, stream))
 
 
 def ep_dispatch_from_host(cfg, layout, h_x, d_x, d_topk_weights, d_recv_x, d_recv_scale,
@@ -432,6 +443,30 @@ def combine(cfg: Config, layout: Layout, expert_out, topk_weights=None, y=None,
                     _ptr(y), _stream(stream))
     _check(st, "ep_combine")
     return y
+
+
+def layout_and_dispatch(cfg: Config, topk_idx, x, topk_weights=None, layout=None,
+                        recv_x=None, recv_scale=None, recv_w=None, want_weights: bool = True,
+                        stream=None):
+    """ep_layout_and_dispatch.  topk_idx: int64 CUDA tensor [T, K]; x: bf16 CUDA
+    tensor [T, H].  Returns (layout, recv_x, recv_scale, recv_w)."""
+    import torch
+
+    cap, H = cfg.capacity, cfg.hidden
+    dev = x.device
+    L = layout or Layout(cfg, device=dev)
+    if recv_x is None:
+        dt = torch.uint8 if cfg.use_fp8_dispatch else torch.bfloat16
+        recv_x = torch.empty((cap, H), dtype=dt, device=dev)
+    if cfg.use_fp8_dispatch and recv_scale is None:
+        recv_scale = torch.empty((cap, H // 128), dtype=torch.float32, device=dev)
+    if want_weights and topk_weights is not None and recv_w is None:
+        recv_w = torch.empty(cap, dtype=torch.float32, device=dev)
+    st = ep_layout_and_dispatch(cfg.c(), topk_idx.shape[0], _ptr(topk_idx), L.c, _ptr(x),
+                                _ptr(topk_weights), _ptr(recv_x), _ptr(recv_scale),
+                                _ptr(recv_w), _stream(stream))
+    _check(st, "ep_layout_and_dispatch")
+    return L, recv_x, recv_scale, recv_w
 
 
 def dispatch_from_host(cfg: Config, layout: Layout, h_x, d_x=None, topk_weights=None,

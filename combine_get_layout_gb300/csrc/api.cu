@@ -134,44 +134,52 @@ int64_t ep_layout_workspace_bytes(const ep_config* cfg) {
   return layout_workspace_bytes(cfg->num_experts, cfg->num_ranks);
 }
 
-int32_t ep_get_layout(const ep_config* cfg, int32_t num_tokens,
-                      const int64_t* d_topk_idx, ep_layout* layout,
-                      int32_t* h_expert_count, void* stream) {
+// Checks the arguments of a layout call and fills its launch arguments.
+static int32_t layout_args(const ep_config* cfg, int32_t num_tokens,
+                           const int64_t* d_topk_idx, const ep_layout* layout, LayoutArgs* a) {
   if (!config_ok(cfg) || !layout_ptrs_ok(layout)) return EP_ERR_INVALID_ARG;
   if (num_tokens < 0 || num_tokens > cfg->max_tokens) return EP_ERR_INVALID_ARG;
   if (num_tokens > 0 && (d_topk_idx == nullptr || !aligned16(d_topk_idx)))
     return EP_ERR_INVALID_ARG;
   const int K = cfg->num_topk, E = cfg->num_experts, R = cfg->num_ranks;
-  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
+  a->topk_idx = d_topk_idx;
+  a->T = num_tokens;
+  a->K = K;
+  a->E = E;
+  a->R = R;
+  a->A = cfg->expert_alignment;
+  a->geom = layout_tiles(num_tokens > 0 ? num_tokens : 1, K);
+  if (a->geom.num_tiles > kLayoutMaxTiles) return EP_ERR_INVALID_ARG;
+  a->ws = carve_layout_workspace(layout->workspace, E, R);
+  a->expert_count = layout->expert_count;
+  a->expert_start = layout->expert_start;
+  a->expert_end = layout->expert_end;
+  a->rank_start = layout->rank_start;
+  a->tokens_per_rank = layout->tokens_per_rank;
+  a->slot_of = layout->slot_of;
+  a->src_info = layout->src_info;
+  a->err = layout->err;
+  a->is_token_in_rank = layout->is_token_in_rank;
+  a->rank_row_start = layout->rank_row_start;
+  a->rank_slot_of = layout->rank_slot_of;
+  a->rank_src = layout->rank_src;
+  return EP_OK;
+}
+
+int32_t ep_get_layout(const ep_config* cfg, int32_t num_tokens,
+                      const int64_t* d_topk_idx, ep_layout* layout,
+                      int32_t* h_expert_count, void* stream) {
   LayoutArgs a;
-  a.topk_idx = d_topk_idx;
-  a.T = num_tokens;
-  a.K = K;
-  a.E = E;
-  a.R = R;
-  a.A = cfg->expert_alignment;
-  a.geom = layout_tiles(num_tokens > 0 ? num_tokens : 1, K);
-  if (a.geom.num_tiles > kLayoutMaxTiles) return EP_ERR_INVALID_ARG;
-  a.ws = carve_layout_workspace(layout->workspace, E, R);
-  a.expert_count = layout->expert_count;
-  a.expert_start = layout->expert_start;
-  a.expert_end = layout->expert_end;
-  a.rank_start = layout->rank_start;
-  a.tokens_per_rank = layout->tokens_per_rank;
-  a.slot_of = layout->slot_of;
-  a.src_info = layout->src_info;
-  a.err = layout->err;
-  a.is_token_in_rank = layout->is_token_in_rank;
-  a.rank_row_start = layout->rank_row_start;
-  a.rank_slot_of = layout->rank_slot_of;
-  a.rank_src = layout->rank_src;
+  const int32_t v = layout_args(cfg, num_tokens, d_topk_idx, layout, &a);
+  if (v != EP_OK) return v;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = note_cuda(launch_layout(a, s));
   if (e != cudaSuccess) return EP_ERR_CUDA;
   layout->num_tokens = num_tokens;
   if (h_expert_count != nullptr) {
     int32_t bits = 0;
-    e = cudaMemcpyAsync(h_expert_count, layout->expert_count, sizeof(int32_t) * E,
+    e = cudaMemcpyAsync(h_expert_count, layout->expert_count, sizeof(int32_t) * a.E,
                         cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(&bits, layout->err, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
@@ -182,12 +190,12 @@ int32_t ep_get_layout(const ep_config* cfg, int32_t num_tokens,
   return EP_OK;
 }
 
-int32_t ep_dispatch(const ep_config* cfg, const ep_layout* layout,
-                    const void* d_x, const float* d_topk_weights,
-                    void* d_recv_x, float* d_recv_scale, float* d_recv_w,
-                    void* stream) {
+// Checks the arguments of a dispatch of T tokens and fills its launch
+// arguments.
+static int32_t dispatch_args(const ep_config* cfg, const ep_layout* layout, int T,
+                             const void* d_x, const float* d_topk_weights, void* d_recv_x,
+                             float* d_recv_scale, float* d_recv_w, DispatchArgs* a) {
   if (!config_ok(cfg) || !layout_ptrs_ok(layout)) return EP_ERR_INVALID_ARG;
-  const int T = layout->num_tokens;
   if (T < 0 || T > cfg->max_tokens) return EP_ERR_INVALID_ARG;
   if (d_recv_x == nullptr || !aligned16(d_recv_x)) return EP_ERR_INVALID_ARG;
   if (T > 0 && (d_x == nullptr || !aligned16(d_x))) return EP_ERR_INVALID_ARG;
@@ -196,24 +204,54 @@ int32_t ep_dispatch(const ep_config* cfg, const ep_layout* layout,
   if (d_recv_w != nullptr && d_topk_weights == nullptr) return EP_ERR_INVALID_ARG;
   if (cfg->use_fp8_dispatch && (d_recv_scale == nullptr || !aligned16(d_recv_scale)))
     return EP_ERR_INVALID_ARG;
-  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
+  a->x = d_x;
+  a->topk_weights = d_topk_weights;
+  a->slot_of = layout->slot_of;
+  a->expert_start = layout->expert_start;
+  a->expert_end = layout->expert_end;
+  a->T = T;
+  a->H = cfg->hidden;
+  a->K = cfg->num_topk;
+  a->E = cfg->num_experts;
+  a->fp8 = cfg->use_fp8_dispatch != 0;
+  a->zero_padding = cfg->zero_padding != 0;
+  a->recv_x = d_recv_x;
+  a->recv_scale = d_recv_scale;
+  a->recv_w = d_recv_w;
+  a->err = layout->err;
+  return EP_OK;
+}
+
+int32_t ep_dispatch(const ep_config* cfg, const ep_layout* layout,
+                    const void* d_x, const float* d_topk_weights,
+                    void* d_recv_x, float* d_recv_scale, float* d_recv_w,
+                    void* stream) {
+  if (layout == nullptr) return EP_ERR_INVALID_ARG;
   DispatchArgs a;
-  a.x = d_x;
-  a.topk_weights = d_topk_weights;
-  a.slot_of = layout->slot_of;
-  a.expert_start = layout->expert_start;
-  a.expert_end = layout->expert_end;
-  a.T = T;
-  a.H = cfg->hidden;
-  a.K = cfg->num_topk;
-  a.E = cfg->num_experts;
-  a.fp8 = cfg->use_fp8_dispatch != 0;
-  a.zero_padding = cfg->zero_padding != 0;
-  a.recv_x = d_recv_x;
-  a.recv_scale = d_recv_scale;
-  a.recv_w = d_recv_w;
-  a.err = layout->err;
+  const int32_t v = dispatch_args(cfg, layout, layout->num_tokens, d_x, d_topk_weights,
+                                  d_recv_x, d_recv_scale, d_recv_w, &a);
+  if (v != EP_OK) return v;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
   return cuda_status(launch_dispatch(a, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t ep_layout_and_dispatch(const ep_config* cfg, int32_t num_tokens,
+                               const int64_t* d_topk_idx, ep_layout* layout,
+                               const void* d_x, const float* d_topk_weights,
+                               void* d_recv_x, float* d_recv_scale, float* d_recv_w,
+                               void* stream) {
+  LayoutArgs la;
+  int32_t v = layout_args(cfg, num_tokens, d_topk_idx, layout, &la);
+  if (v != EP_OK) return v;
+  DispatchArgs da;
+  v = dispatch_args(cfg, layout, num_tokens, d_x, d_topk_weights, d_recv_x, d_recv_scale,
+                    d_recv_w, &da);
+  if (v != EP_OK) return v;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
+  const cudaError_t e = note_cuda(launch_layout_dispatch(la, da, static_cast<cudaStream_t>(stream)));
+  if (e != cudaSuccess) return EP_ERR_CUDA;
+  layout->num_tokens = num_tokens;
+  return EP_OK;
 }
 
 int32_t ep_combine(const ep_config* cfg, const ep_layout* layout,

@@ -42,7 +42,6 @@ __global__ void __launch_bounds__(256)
   const int per = (nvec + slices - 1) / slices;
   const int v0 = slice * per, v1 = min(nvec, v0 + per);
   pdl_wait();
-  pdl_launch_dependents();
   if (tid < 32) {
     // warp 0 reads the route and compacts the used selections (a sparse
     // route -- e.g. a token's few ranks out of many -- then costs one batch
@@ -173,7 +172,6 @@ __global__ void __launch_bounds__(256)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nvec = H >> 3;
   pdl_wait();
-  pdl_launch_dependents();
   if (tid < K) {
     s_slot[tid] = slot_of[int64_t(t) * K + tid];
     s_w[tid] = w != nullptr ? w[int64_t(t) * K + tid] : 1.0f;

@@ -10,6 +10,7 @@
 // of its rows.
 #include "ep_device.cuh"
 #include "ep_internal.h"
+#include "fp8_quant.cuh"
 
 namespace ep {
 
@@ -35,7 +36,6 @@ __global__ void __launch_bounds__(512)
   const int t = blockIdx.x;
   const int tid = threadIdx.x;
   pdl_wait();
-  pdl_launch_dependents();
   const uint4* row = x + int64_t(t) * nvec;
   const int v0 = first_vec();
   uint4 first = make_uint4(0, 0, 0, 0);
@@ -67,24 +67,6 @@ __device__ __forceinline__ int64_t scale_index(int64_t row, int blk, int nblk, i
   return kColMajor ? int64_t(blk) * ld + row : row * nblk + blk;
 }
 
-// x / s for a block scale s >= kFastScaleMin and |x| <= 448 s, given
-// y = RN(1/s): q0 = x * y, then one correction with the exact residual
-// r = x - q0 * s (one FMA), after Markstein's FMA-based division
-// (P. Markstein, "IA-64 and Elementary Functions", 2000).  The reciprocal
-// is taken once per block.  The quotient can differ from the IEEE one in
-// the last fp32 bit, but never in the E4M3 code it rounds to: the inputs
-// here are bf16 values and the scale of a bf16 block maximum, and
-// ep_selftest_fp8_quotient compares the codes against those of the IEEE
-// division over that whole domain (every bf16 maximum, every bf16 value).
-constexpr float kFastScaleMin = 0x1p-100f;
-
-__device__ __forceinline__ float scaled_quotient(float x, float s, float y) {
-  const float q0 = x * y;
-  const float r = fmaf(-q0, s, x);
-  // s > 0: the quotient has x's sign (the correction would turn -0 into +0)
-  return copysignf(fmaf(r, y, q0), x);
-}
-
 // One CTA per token; thread u owns 16 consecutive channels (two 16-byte
 // loads), so 8 lanes cover one 128-channel block: exact amax by three
 // shuffles, scale = amax / 448, 16 E4M3 bytes written with one 16-byte store
@@ -104,7 +86,6 @@ __global__ void __launch_bounds__(1024)
   const int n16 = H >> 4;      // 16-channel groups per row
   const int nblk = H >> 7;     // 128-channel scale blocks per row
   pdl_wait();
-  pdl_launch_dependents();
   if (tid < K) {
     const int sl = slot_of[int64_t(t) * K + tid];
     s_slot[tid] = sl;
@@ -123,37 +104,9 @@ __global__ void __launch_bounds__(1024)
       r0 = ld_stream_u4(x + int64_t(t) * nvec + 2 * u);
       r1 = ld_stream_u4(x + int64_t(t) * nvec + 2 * u + 1);
     }
-    const float f[16] = {bf16_lo(r0.x), bf16_hi(r0.x), bf16_lo(r0.y), bf16_hi(r0.y),
-                         bf16_lo(r0.z), bf16_hi(r0.z), bf16_lo(r0.w), bf16_hi(r0.w),
-                         bf16_lo(r1.x), bf16_hi(r1.x), bf16_lo(r1.y), bf16_hi(r1.y),
-                         bf16_lo(r1.z), bf16_hi(r1.z), bf16_lo(r1.w), bf16_hi(r1.w)};
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
-#pragma unroll
-    for (int o = 4; o >= 1; o >>= 1)
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    uint4 q = make_uint4(0, 0, 0, 0);
-    float scale = 0.0f;
-    if (amax != 0.0f) {
-      scale = __fdiv_rn(amax, 448.0f);
-      uint32_t p[8];
-      if (scale >= kFastScaleMin) {
-        const float y = __frcp_rn(scale);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          p[j] = pack_e4m3x2(scaled_quotient(f[2 * j], scale, y),
-                             scaled_quotient(f[2 * j + 1], scale, y));
-      } else {  // 1 / scale would overflow: divide
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          p[j] = pack_e4m3x2(__fdiv_rn(f[2 * j], scale), __fdiv_rn(f[2 * j + 1], scale));
-      }
-      q.x = p[0] | (p[1] << 16);
-      q.y = p[2] | (p[3] << 16);
-      q.z = p[4] | (p[5] << 16);
-      q.w = p[6] | (p[7] << 16);
-    }
+    uint4 q;
+    float scale;
+    quantize_group16(r0, r1, &q, &scale);
     if (active) {
       const bool leader = (tid & 7) == 0;
       for (int k = 0; k < K; ++k) {
@@ -184,7 +137,6 @@ __global__ void __launch_bounds__(1024)
   const int n16 = H >> 4;      // 16-byte vectors of E4M3 per row
   const int nblk = H >> 7;
   pdl_wait();
-  pdl_launch_dependents();
   if (tid < K) {
     const int sl = slot_of[int64_t(t) * K + tid];
     s_slot[tid] = sl;
@@ -219,7 +171,6 @@ __global__ void __launch_bounds__(256)
                         float* __restrict__ recv_scale,
                         float* __restrict__ recv_w) {
   pdl_wait();
-  pdl_launch_dependents();
   for (int e = blockIdx.x; e < E; e += gridDim.x) {
     const int64_t s0 = expert_end[e], s1 = expert_start[e + 1];
     if (s1 <= s0) continue;
@@ -243,7 +194,6 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(32) wait_selftest_kernel(uint64_t timeout_ns, int32_t* err) {
   __shared__ __align__(8) uint64_t bar;
   pdl_wait();
-  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();

@@ -27,6 +27,8 @@ constexpr int kScanChunkInts = 8192;
 constexpr int kSmallLayoutPairs = 4096;
 constexpr int kSmallLayoutMaxExperts = 2048;
 bool layout_is_small(int64_t T, int K, int E);
+// Pairs a CTA of the one-launch layout may own when it also dispatches them.
+constexpr int kSmallOwnPairs = 64;
 
 
 struct TileGeom {
@@ -71,6 +73,16 @@ struct LayoutArgs {
 };
 
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream);
+
+// Dispatch work handed to the one-launch layout (layout_small_kernel).
+struct SmallDispatch {
+  const uint4* x = nullptr;       // bf16 [T, H]
+  const float* w = nullptr;       // [T, K] or null
+  void* recv_x = nullptr;         // bf16 or E4M3 rows
+  float* recv_scale = nullptr;    // [cap, H/128] row-major (E4M3)
+  float* recv_w = nullptr;        // [cap] or null
+  int H = 0;
+};
 
 struct DispatchArgs {
   const void* x;
@@ -147,6 +159,12 @@ struct RankArgs {
 };
 
 cudaError_t launch_ranks(const RankArgs& a, cudaStream_t stream);
+
+// Layout then dispatch; for small inputs one launch does both (the CTAs of
+// the one-launch layout dispatch their own tokens), else the two paths run
+// in turn.  Results equal launch_layout followed by launch_dispatch.
+cudaError_t launch_layout_dispatch(const LayoutArgs& la, const DispatchArgs& da,
+                                   cudaStream_t stream);
 
 // Threads per CTA and CTAs per token (grid.y) for a row of nvec vectors: the
 // fewest CTAs of at most `cap` threads, balanced, in whole warps.  Several

@@ -22,6 +22,7 @@
 //      publishes the per-expert arrays; rank totals are spread over CTAs.
 #include "ep_device.cuh"
 #include "ep_internal.h"
+#include "fp8_quant.cuh"
 
 namespace ep {
 
@@ -580,7 +581,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
 // kernel, rows for its own few tokens in (t, k) order, rank rows and
 // padding.  The rows are the same as the two-launch path's.
 struct SmallSmem {
-  int idx, hist, start, total, base, rcnt, rstart, scr, bytes;
+  int idx, hist, start, total, base, rcnt, rstart, scr, own, bytes;
 };
 
 __host__ __device__ inline SmallSmem small_smem(int E, int R) {
@@ -595,6 +596,7 @@ __host__ __device__ inline SmallSmem small_smem(int E, int R) {
   s.rcnt = o;   o += 3 * Rpad * 4;                 // rank counts, same regions
   s.rstart = o; o += ((R + 1 + 3) & ~3) * 4;
   s.scr = o;    o += 36 * 4;                       // scan scratch, [33] = errors
+  s.own = o;    o += kSmallOwnPairs * 4;           // rows of this CTA's pairs
   s.bytes = o;
   return s;
 }
@@ -602,9 +604,14 @@ __host__ __device__ inline SmallSmem small_smem(int E, int R) {
 // CTAs of the one-launch layout (each owns about T / kSmallLayoutCtas tokens).
 constexpr int kSmallLayoutCtas = kLayoutMaxTiles;
 
+// kMode: 0 layout only; 1 and 2 also dispatch each CTA's own tokens, as
+// bf16 rows (1) or E4M3 rows with row-major 1x128 scales (2) -- the same
+// rows and values as dispatch_bf16_kernel / dispatch_fp8_kernel write.
+template <int kMode>
 __global__ void __launch_bounds__(kLayoutThreads)
     layout_small_kernel(const int64_t* __restrict__ topk_idx, int T, int K, int E,
-                        int R, int A, uint8_t* __restrict__ is_token_in_rank,
+                        int R, int A, SmallDispatch d,
+                        uint8_t* __restrict__ is_token_in_rank,
                         int32_t* __restrict__ expert_count,
                         int32_t* __restrict__ expert_start,
                         int32_t* __restrict__ expert_end,
@@ -627,6 +634,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
   int32_t* rcnt = reinterpret_cast<int32_t*>(smem + L.rcnt);      // [3][Rpad]
   int32_t* s_rstart = reinterpret_cast<int32_t*>(smem + L.rstart);
   int32_t* s_scr = reinterpret_cast<int32_t*>(smem + L.scr);
+  int32_t* s_own = reinterpret_cast<int32_t*>(smem + L.own);       // [kSmallOwnPairs]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int2* src_info2 = reinterpret_cast<int2*>(src_info);
 
@@ -725,6 +733,11 @@ __global__ void __launch_bounds__(kLayoutThreads)
           const int tl = p / K;
           src_info2[slot] = make_int2(ctb + tl, p - tl * K);
         }
+        if (kMode != 0) {
+          s_own[p] = slot;
+          if (slot >= 0 && d.w != nullptr && d.recv_w != nullptr)
+            d.recv_w[slot] = d.w[int64_t(ctb) * K + p];
+        }
       }
     }
   }
@@ -783,6 +796,52 @@ __global__ void __launch_bounds__(kLayoutThreads)
     const int s0 = s_start[e] + s_total[e], s1 = s_start[e + 1];
     for (int s = s0 + lane; s < s1; s += 32) src_info2[s] = make_int2(-1, -1);
   }
+
+  if (kMode == 0) return;
+  // Dispatch of this CTA's own tokens to the rows just assigned.
+  __syncthreads();
+  const int nt = cte - ctb;
+  const int nvec = d.H >> 3;
+  if (kMode == 1) {
+    uint4* rx = static_cast<uint4*>(d.recv_x);
+    for (int i = 0; i < nt; ++i) {
+      const uint4* row = d.x + int64_t(ctb + i) * nvec;
+      for (int v = tid; v < nvec; v += blockDim.x) {
+        const uint4 r = ld_stream_u4(row + v);
+        for (int k = 0; k < K; ++k) {
+          const int sl = s_own[i * K + k];
+          if (sl >= 0) rx[int64_t(sl) * nvec + v] = r;
+        }
+      }
+    }
+  } else {
+    // 8 aligned lanes per 128-channel block (blockDim is a multiple of 32)
+    uint8_t* rq = static_cast<uint8_t*>(d.recv_x);
+    const int n16 = d.H >> 4, nblk = d.H >> 7;
+    for (int i = 0; i < nt; ++i) {
+      const uint4* row = d.x + int64_t(ctb + i) * nvec;
+      for (int base = 0; base < n16; base += blockDim.x) {
+        const int u = base + tid;
+        const bool active = u < n16;
+        uint4 r0 = make_uint4(0, 0, 0, 0), r1 = r0;
+        if (active) {
+          r0 = ld_stream_u4(row + 2 * u);
+          r1 = ld_stream_u4(row + 2 * u + 1);
+        }
+        uint4 q;
+        float scale;
+        quantize_group16(r0, r1, &q, &scale);
+        if (!active) continue;
+        const bool leader = (tid & 7) == 0;
+        for (int k = 0; k < K; ++k) {
+          const int sl = s_own[i * K + k];
+          if (sl < 0) continue;
+          *reinterpret_cast<uint4*>(rq + int64_t(sl) * d.H + int64_t(u) * 16) = q;
+          if (leader) d.recv_scale[int64_t(sl) * nblk + (u >> 3)] = scale;
+        }
+      }
+    }
+  }
 }
 
 static int count_smem(int E, int R, int K) {
@@ -793,7 +852,9 @@ static int count_smem(int E, int R, int K) {
 cudaError_t prepare_layout_kernels() {
   const int optin = device_info().max_smem_optin;
   cudaError_t st = allow_max_dynamic_smem(layout_count_kernel, optin);
-  if (st == cudaSuccess) st = allow_max_dynamic_smem(layout_small_kernel, optin);
+  if (st == cudaSuccess) st = allow_max_dynamic_smem(layout_small_kernel<0>, optin);
+  if (st == cudaSuccess) st = allow_max_dynamic_smem(layout_small_kernel<1>, optin);
+  if (st == cudaSuccess) st = allow_max_dynamic_smem(layout_small_kernel<2>, optin);
   if (st != cudaSuccess) return st;
   return allow_max_dynamic_smem(layout_assign_kernel, optin);
 }
@@ -804,9 +865,9 @@ bool layout_is_small(int64_t T, int K, int E) {
 
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
   if (layout_is_small(a.T, a.K, a.E)) {
-    return launch_pdl(layout_small_kernel, dim3(kSmallLayoutCtas), dim3(kLayoutThreads),
+    return launch_pdl(layout_small_kernel<0>, dim3(kSmallLayoutCtas), dim3(kLayoutThreads),
                       small_smem(a.E, a.R).bytes, stream, a.topk_idx, a.T, a.K, a.E, a.R,
-                      a.A, a.is_token_in_rank, a.expert_count, a.expert_start,
+                      a.A, SmallDispatch{}, a.is_token_in_rank, a.expert_count, a.expert_start,
                       a.expert_end, a.rank_start, a.tokens_per_rank, a.slot_of, a.src_info,
                       a.rank_row_start, a.rank_slot_of, a.rank_src, a.err);
   }
@@ -833,6 +894,40 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
                     a.expert_start, a.expert_end, a.rank_start, a.tokens_per_rank,
                     a.slot_of, a.src_info, a.rank_row_start, a.rank_slot_of,
                     a.rank_src, a.err);
+}
+
+// Rows of the pairs one CTA of the one-launch layout owns, at most.
+static bool small_fusable(int T, int K) {
+  const int tt = (T + kSmallLayoutCtas - 1) / kSmallLayoutCtas;
+  return tt * K <= kSmallOwnPairs;
+}
+
+cudaError_t launch_layout_dispatch(const LayoutArgs& la, const DispatchArgs& da,
+                                   cudaStream_t stream) {
+  const bool fuse = la.T > 0 && layout_is_small(la.T, la.K, la.E) && small_fusable(la.T, la.K) &&
+                    da.x_q == nullptr && !da.scale_col_major;
+  if (!fuse) {
+    cudaError_t st = launch_layout(la, stream);
+    return st != cudaSuccess ? st : launch_dispatch(da, stream);
+  }
+  SmallDispatch d;
+  d.x = static_cast<const uint4*>(da.x);
+  d.w = da.topk_weights;
+  d.recv_x = da.recv_x;
+  d.recv_scale = da.recv_scale;
+  d.recv_w = da.recv_w;
+  d.H = da.H;
+  auto kern = da.fp8 ? layout_small_kernel<2> : layout_small_kernel<1>;
+  cudaError_t st = launch_pdl(kern, dim3(kSmallLayoutCtas), dim3(kLayoutThreads),
+                              small_smem(la.E, la.R).bytes, stream, la.topk_idx, la.T, la.K,
+                              la.E, la.R, la.A, d, la.is_token_in_rank, la.expert_count,
+                              la.expert_start, la.expert_end, la.rank_start,
+                              la.tokens_per_rank, la.slot_of, la.src_info, la.rank_row_start,
+                              la.rank_slot_of, la.rank_src, la.err);
+  if (st != cudaSuccess || !da.zero_padding) return st;
+  DispatchArgs z = da;   // the alignment gap rows, as ep_dispatch clears them
+  z.T = 0;
+  return launch_dispatch(z, stream);
 }
 
 }  // namespace ep

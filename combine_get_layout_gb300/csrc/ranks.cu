@@ -64,7 +64,6 @@ __global__ void __launch_bounds__(512)
   const int t = blockIdx.x;
   const int tid = threadIdx.x;
   pdl_wait();
-  pdl_launch_dependents();
   const uint4* row = x + int64_t(t) * nvec;
   const int v0 = first_vec();
   uint4 first = make_uint4(0, 0, 0, 0);
@@ -120,7 +119,6 @@ __global__ void __launch_bounds__(512)
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
   pdl_wait();
-  pdl_launch_dependents();
   for (int j = tid; j < G * K; j += blockDim.x) {
     const int g = j / K, k = j - g * K;
     const int t = t0 + g;
@@ -207,7 +205,6 @@ __global__ void __launch_bounds__(256)
   const int t = blockIdx.x;
   const int tid = threadIdx.x;
   pdl_wait();
-  pdl_launch_dependents();
   if (tid < K) {
     const int64_t e = topk_idx[int64_t(t) * K + tid];
     const int s = slot_of[int64_t(t) * K + tid];

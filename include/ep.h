@@ -194,6 +194,25 @@ EP_API int32_t ep_combine(const ep_config *cfg, const ep_layout *layout,
                    const void *d_expert_out, const float *d_topk_weights,
                    void *d_y, void *stream);
 
+/* Layout and dispatch in one call ("Deep Dive - DeepEP", "Dispatch: layout,
+ * move, and epilogue": a dispatch counts and lays out rows by rank and
+ * expert, then moves them -- conceptual stages that kernels can overlap).
+ *
+ * Same arguments and results as ep_get_layout (with h_expert_count NULL)
+ * followed by ep_dispatch of the same num_tokens tokens, and the same errors
+ * for the same arguments.  For inputs of at most 4096 (t, k) pairs whose
+ * one-launch layout gives each of its CTAs at most 64 pairs, one kernel does
+ * both: each CTA of the layout dispatches its own tokens as soon as their
+ * rows are known, so the dispatch costs no second launch.  Larger inputs
+ * run the two paths in turn.  (Column-major scales and pre-quantised input
+ * are ep_dispatch_fp8's and are not offered here.)  Returns EP_OK or an
+ * error. */
+EP_API int32_t ep_layout_and_dispatch(const ep_config *cfg, int32_t num_tokens,
+                                      const int64_t *d_topk_idx, ep_layout *layout,
+                                      const void *d_x, const float *d_topk_weights,
+                                      void *d_recv_x, float *d_recv_scale,
+                                      float *d_recv_w, void *stream);
+
 /* Allocation-free layout.  The pages have no counterpart: this entry point
  * exists for callers that cannot allocate device memory -- code inside a
  * framework that owns all device memory and has no spare buffer to give, a

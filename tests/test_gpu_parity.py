@@ -509,3 +509,35 @@ def test_extreme_configs_whole_path(ep, name, zp):
     ref_y = oracle.combine(host_u16(Y), inp["topk_weights"], ora["slot_of"])
     assert np.array_equal(host_u16(y), ref_y)
 
+
+# --------------------------------------------------------------------------
+# layout and dispatch in one call: fused for small inputs, the two paths in
+# turn for larger ones -- the same layout and rows as separate calls
+# --------------------------------------------------------------------------
+
+FUSED = ["tiny", "decode", "ragged_fp8", "small_edge", "k1_e_eq_r", "wide_ranks_small",
+         "k_eq_e", "one_token_bf16", "one_token_fp8", "past_small_edge", "prefill"]
+
+
+@pytest.mark.parametrize("name", FUSED)
+@pytest.mark.parametrize("zp", [False, True])
+def test_layout_and_dispatch_equals_separate_calls(ep, name, zp):
+    wl = workloads.WORKLOADS.get(name) or MEDIUM.get(name) or EXTREME[name]
+    inp = inputs(wl)
+    cfg = cfg_of(ep, wl, zero_padding=zp)
+    idx, x, w = dev(inp["topk_idx"]), dev_bf16(inp["x"]), dev(inp["topk_weights"])
+    L1 = ep.get_layout(cfg, idx, sync=True)
+    rx1, rs1, rw1 = ep.dispatch(cfg, L1, x, w)
+    L2, rx2, rs2, rw2 = ep.layout_and_dispatch(cfg, idx, x, w)
+    torch.cuda.synchronize()
+    assert ep.check_error(L2) == ep.EP_OK
+    ora = oracle_layout(wl, inp["topk_idx"], cfg.capacity)
+    assert_layout_equal(L2, ora, wl.num_tokens)
+    used = int(ora["expert_start"][-1])
+    rows = np.arange(used) if zp else np.nonzero(ora["src_info"][:used, 0] >= 0)[0]
+    r = torch.from_numpy(rows).long().cuda()
+    assert torch.equal(rx2[r].view(torch.uint8), rx1[r].view(torch.uint8))
+    if cfg.use_fp8_dispatch:
+        assert torch.equal(rs2[r].view(torch.int32), rs1[r].view(torch.int32))
+    assert torch.equal(rw2[r].view(torch.int32), rw1[r].view(torch.int32))
+
