@@ -37,23 +37,16 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 
 // ---- programmatic dependent launch ----------------------------------------
 // Every kernel of the library is launched with programmatic stream
-// serialisation.  It waits for the preceding grid (griddepcontrol.wait)
+// serialisation and waits for the preceding grid (griddepcontrol.wait)
 // before its first read of global memory that another kernel may have
-// written, and only after that wait lets the next grid start launching, so
-// that when a kernel of this library passes its own wait, every grid before
-// its predecessor has completed as well.  The short layout kernels let the
-// next grid launch right after their wait; the long streaming kernels
-// (dispatch, combine and the rank stage) do not signal at all, so their
-// dependents launch as their CTAs exit: early-launched CTAs of the next grid
-// would hold warp slots through a long kernel's last waves (measured at 16K
-// tokens: a step of 687 us with the early signal, 646 us without).
+// written.  None signals its dependents early: the next grid starts
+// launching as this one's CTAs exit, which still hides the launch gap.  An
+// early signal let waiting CTAs of the next grid hold warp slots while this
+// grid ran (measured, same box: prefill step 178 -> 174 us, skew
+// 134 -> 128 us, 16K-token FP8 step 544 -> 518 us without it).
 
 __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---- mbarrier -----------------------------------------------------------

@@ -181,7 +181,6 @@ __global__ void __launch_bounds__(kLayoutThreads)
   for (int e = tid; e < Wc; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   pdl_wait();
-  pdl_launch_dependents();
 
   const int tile = blockIdx.x;
   const int t0 = tile * tile_tokens;
@@ -334,7 +333,6 @@ __global__ void __launch_bounds__(kLayoutThreads)
   }
   __syncthreads();
   pdl_wait();
-  pdl_launch_dependents();
 
   // Stream the tile-count matrix through two shared-memory buffers.
   const int rows = L.chunk_rows;
@@ -643,7 +641,6 @@ __global__ void __launch_bounds__(kLayoutThreads)
   if (tid == 0) s_scr[33] = 0;
   __syncthreads();
   pdl_wait();
-  pdl_launch_dependents();
 
   // This CTA's tokens [ctb, cte).
   const int tt = (T + gridDim.x - 1) / gridDim.x;
