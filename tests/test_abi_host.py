@@ -125,6 +125,17 @@ def test_null_and_misaligned_pointers_rejected(ep):
                                  None) == ep.EP_ERR_INVALID_ARG
     assert ep.ep_combine_to_host(cfg, lay, 0x40000, None, None, 0x60000, 4,
                                  None) == ep.EP_ERR_INVALID_ARG
+    # layout and dispatch in one call: the checks of both calls
+    assert ep.ep_layout_and_dispatch(cfg, 4, None, lay, 0x30000, None, 0x40000, None, None,
+                                     None) == ep.EP_ERR_INVALID_ARG          # no routes
+    assert ep.ep_layout_and_dispatch(cfg, 4, 0x20000, lay, None, None, 0x40000, None, None,
+                                     None) == ep.EP_ERR_INVALID_ARG          # no x
+    assert ep.ep_layout_and_dispatch(cfg, 17, 0x20000, lay, 0x30000, None, 0x40000, None,
+                                     None, None) == ep.EP_ERR_INVALID_ARG    # > max_tokens
+    assert ep.ep_layout_and_dispatch(cfg8, 4, 0x20000, lay, 0x30000, None, 0x40000, None,
+                                     None, None) == ep.EP_ERR_INVALID_ARG    # fp8, no scales
+    assert ep.ep_layout_and_dispatch(cfg, 4, 0x20000, lay, 0x30000, None, 0x40000, None,
+                                     0x50000, None) == ep.EP_ERR_INVALID_ARG  # recv_w, no w
 
 
 def test_status_strings(ep):
