@@ -311,7 +311,8 @@ def _fp8_oracle_rows(x_rows):
 
 @pytest.mark.parametrize("name,zp", [("decode", False), ("ragged_fp8", True),
                                      ("ragged_fp8", False), ("wide_experts", True),
-                                     ("skew_small", False), ("skew", False)])
+                                     ("skew_small", False), ("skew", False),
+                                     ("sweep1k_fp8", False), ("sweep16k_fp8", False)])
 def test_dispatch_fp8_bit_exact(ep, name, zp):
     wl = workloads.WORKLOADS.get(name) or MEDIUM[name]
     inp, cfg, L, ora, recv_q, recv_s, recv_w = _dispatch_case(ep, wl, zp)
