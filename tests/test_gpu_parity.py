@@ -121,6 +121,14 @@ MEDIUM = {
     "skew_small": workloads.Workload("skew_small", 700, 512, 64, 6, 8, True,
                                      zipf_alpha=1.2, mask_frac=0.05),
     "many_tiles": workloads.Workload("many_tiles", 70000, 8, 256, 8, 8, False),
+    # the largest expert and rank counts: count rows of 4096 entries,
+    # streamed two rows at a time; byte-wise rank flags
+    "max_experts_ranks": workloads.Workload("max_experts_ranks", 1000, 128, 2048, 8, 2048,
+                                            False, expert_alignment=4, mask_frac=0.05),
+    # one expert, past the one-launch limit: 8-entry count rows, most row
+    # groups of the column sums empty
+    "one_expert_big": workloads.Workload("one_expert_big", 5000, 64, 1, 1, 1, False,
+                                         expert_alignment=1),
     # 2048 experts over 31 tiles: the tile-count matrix exceeds shared
     # memory and is streamed through the two-buffer ring
     "ring_scan": workloads.Workload("ring_scan", 1000, 128, 2048, 8, 64, False,
