@@ -659,8 +659,8 @@ __global__ void __launch_bounds__(kLayoutThreads)
 
   // Survey in token-aligned warp steps: lanes [0, TPS*K) hold the pairs of
   // TPS consecutive tokens.  Each lane adds its pair to its region's expert
-  // count, and looks at the earlier selections of its own token (a
-  // broadcast read of one shared row): the same expert again is a repeat;
+  // count, and looks at the earlier selections of its own token (by
+  // shuffles from the token's adjacent lanes): the same expert again is a repeat;
   // no earlier expert on the same rank makes it the token's first on that
   // rank, which adds one to the region's rank count and, for this CTA's own
   // tokens, sets the rank-row flag.
@@ -668,21 +668,26 @@ __global__ void __launch_bounds__(kLayoutThreads)
     const int TPS = 32 / K, SP = TPS * K;
     const int steps = (T + TPS - 1) / TPS;
     const int tl = lane / K, kk = lane - tl * K;
+    const int g0 = tl * K;
     for (int st = warp; st < steps; st += kLayoutWarps) {
       const int t = st * TPS + tl;
       const bool live = lane < SP && t < T;
-      const int32_t* row = s_idx + (st * SP + tl * K);
-      const int e = live ? row[kk] : -1;
+      const int e = live ? s_idx[st * SP + lane] : -1;
+      const int r = e >= 0 ? e / Eg : -1;
+      // the token's selections sit in lanes [g0, g0 + K): read them by
+      // shuffles (lanes past the step read wrapped lanes, unused)
+      bool first = true;
+      for (int j = 0; j < K; ++j) {
+        const int ej = __shfl_sync(0xffffffffu, e, (g0 + j) & 31);
+        const int rj = __shfl_sync(0xffffffffu, r, (g0 + j) & 31);
+        if (j < kk && ej >= 0) {
+          if (ej == e) errbits |= ERRBIT_DUP_EXPERT;
+          if (rj == r) first = false;
+        }
+      }
       if (e < 0) continue;
       const int region = t < ctb ? 0 : (t < cte ? 1 : 2);
       atomicAdd(&hist[region * Epad + e], 1);
-      const int r = e / Eg, lo = r * Eg, hi = lo + Eg;
-      bool first = true;
-      for (int j = 0; j < kk; ++j) {
-        const int ej = row[j];
-        if (ej == e) errbits |= ERRBIT_DUP_EXPERT;
-        if (ej >= lo && ej < hi) first = false;
-      }
       if (first) {
         atomicAdd(&rcnt[region * Rpad + r], 1);
         if (region == 1) is_token_in_rank[int64_t(t) * R + r] = 1;
