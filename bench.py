@@ -85,7 +85,16 @@ def parse_args():
                         "combine over ranks (the non-expanded path)")
     p.add_argument("--e2e-chunks", type=int, default=8,
                    help="token chunks of the host-buffer entry points in the e2e leg "
-                        "(copies of later chunks overlap the kernels of earlier ones)")
+                        "when they copy (copies of later chunks overlap the kernels of "
+                        "earlier ones)")
+    p.add_argument("--e2e-transfer", choices=["auto", "direct", "chunked", "copies"],
+                   default="auto",
+                   help="e2e leg: direct = the kernels read x from and write y to pinned "
+                        "host memory in place (host-buffer entry points, 0 chunks); "
+                        "chunked = the same entry points copying token chunks; copies = "
+                        "whole-buffer copies on the stream around the device entry points; "
+                        "auto = direct for bf16 rows, else chunked when the rows span two "
+                        "4 MiB chunks, else copies")
     p.add_argument("--fused", action="store_true",
                    help="forward pass: layout and dispatch through ep_layout_and_dispatch "
                         "(one kernel for small inputs)")
@@ -732,14 +741,25 @@ def run_ours(args):
             ident = torch.empty((cap, H), dtype=torch.bfloat16, device=device)
         bf_cfg = ep.Config(T, H, K, wl.num_experts, wl.num_ranks, wl.expert_alignment,
                            False, False).c()
-        # The host-buffer entry points move x and y in token chunks overlapped
-        # with the kernels.  They pay off when the rows span two chunks of at
+        # The host-buffer entry points either let the kernels read x and write
+        # y in pinned host memory in place (direct: each byte crosses the host
+        # link once, no staging) or move the rows in token chunks overlapped
+        # with the kernels, which pays off when the rows span two chunks of at
         # least 4 MiB (below that, copying everything first and launching the
-        # kernels back to back is faster); the epilogue and FP8 input options
+        # kernels back to back is faster).  The epilogue and FP8 input options
         # have device entry points only, so with those the rows are copied
-        # whole too.
-        host_io = not epilogue and not fp8_opts and T * H * 2 >= 2 * (4 << 20)
-        chunks = args.e2e_chunks
+        # whole.  With FP8 rows the identity experts read the bf16 rows of a
+        # second, bf16 dispatch from the staged x, so x is staged.
+        transfer = args.e2e_transfer
+        if epilogue or fp8_opts:
+            transfer = "copies"
+        elif transfer == "direct" and wl.use_fp8_dispatch:
+            transfer = "chunked"
+        elif transfer == "auto":
+            transfer = ("direct" if not wl.use_fp8_dispatch else
+                        "chunked" if T * H * 2 >= 2 * (4 << 20) else "copies")
+        host_io = transfer != "copies"
+        chunks = 0 if transfer == "direct" else args.e2e_chunks
 
         def e2e_step():
             if not host_io:
@@ -748,7 +768,8 @@ def run_ours(args):
             w_d.copy_(w_h, non_blocking=True)
             layout()
             if host_io:
-                st = ep.ep_dispatch_from_host(ccfg, L.c, x_h.data_ptr(), p(x_d), p(w_d),
+                st = ep.ep_dispatch_from_host(ccfg, L.c, x_h.data_ptr(),
+                                              None if chunks == 0 else p(x_d), p(w_d),
                                               p(recv_x), p(recv_s), p(recv_w), chunks, sptr)
                 assert st == 0, ep.ep_status_str(st)
             else:
@@ -757,7 +778,8 @@ def run_ours(args):
                 st = ep.ep_dispatch(bf_cfg, L.c, p(x_d), None, p(ident), None, None, sptr)
                 assert st == 0
             if host_io:
-                st = ep.ep_combine_to_host(ccfg, L.c, p(ident), p(w_d), p(y_d), y_h.data_ptr(),
+                st = ep.ep_combine_to_host(ccfg, L.c, p(ident), p(w_d),
+                                           None if chunks == 0 else p(y_d), y_h.data_ptr(),
                                            chunks, sptr)
                 assert st == 0, ep.ep_status_str(st)
             else:
@@ -784,7 +806,10 @@ def run_ours(args):
                "h2d_bytes_per_step": x_h.numel() * 2 + idx_h.numel() * 8 + w_h.numel() * 4,
                "d2h_bytes_per_step": y_h.numel() * 2, "ms_per_step": e_ms,
                "experts": "identity (combine reads the dispatched bf16 rows)",
-               "transfer": (f"ep_dispatch_from_host / ep_combine_to_host, {chunks} token "
+               "transfer": ("ep_dispatch_from_host / ep_combine_to_host, direct (the "
+                            "kernels read x and write y in pinned host memory)")
+                           if transfer == "direct" else
+                           (f"ep_dispatch_from_host / ep_combine_to_host, {chunks} token "
                             "chunks (copies overlap the kernels)") if host_io else
                            "whole-buffer copies on the stream"}
 

@@ -473,13 +473,14 @@ def dispatch_from_host(cfg: Config, layout: Layout, h_x, d_x=None, topk_weights=
                        recv_x=None, recv_scale=None, recv_w=None, want_weights: bool = True,
                        num_chunks: int = 8, stream=None):
     """ep_dispatch_from_host.  h_x: bf16 CPU tensor [T, H] (pinned for overlap);
-    d_x: CUDA staging tensor [T, H] (allocated when None).  Returns (recv_x,
-    recv_scale, recv_w, d_x)."""
+    d_x: CUDA staging tensor [T, H] (allocated when None).  num_chunks=0: the
+    kernel reads h_x in place (h_x must be pinned; no staging, d_x stays
+    None).  Returns (recv_x, recv_scale, recv_w, d_x)."""
     import torch
 
     cap, H = cfg.capacity, cfg.hidden
     dev = torch.device("cuda", torch.cuda.current_device())
-    if d_x is None:
+    if d_x is None and num_chunks != 0:
         d_x = torch.empty(tuple(h_x.shape), dtype=torch.bfloat16, device=dev)
     if recv_x is None:
         dt = torch.uint8 if cfg.use_fp8_dispatch else torch.bfloat16
@@ -498,13 +499,14 @@ def dispatch_from_host(cfg: Config, layout: Layout, h_x, d_x=None, topk_weights=
 def combine_to_host(cfg: Config, layout: Layout, expert_out, topk_weights=None, h_y=None,
                     d_y=None, num_chunks: int = 8, stream=None):
     """ep_combine_to_host.  Returns (h_y, d_y): h_y a pinned bf16 CPU tensor
-    [T, H], readable once the stream has been synchronised."""
+    [T, H], readable once the stream has been synchronised.  num_chunks=0:
+    the kernel writes h_y in place (h_y must be pinned; d_y stays None)."""
     import torch
 
     T, H = layout.num_tokens, cfg.hidden
     if h_y is None:
         h_y = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    if d_y is None:
+    if d_y is None and num_chunks != 0:
         d_y = torch.empty((T, H), dtype=torch.bfloat16, device=expert_out.device)
     st = ep_combine_to_host(cfg.c(), layout.c, _ptr(expert_out), _ptr(topk_weights), _ptr(d_y),
                             _ptr(h_y), num_chunks, _stream(stream))

@@ -319,6 +319,18 @@ static int chunk_tokens(int T, int chunks, int64_t row_bytes) {
   return int((T + n - 1) / n);
 }
 
+// The device address of page-locked host memory (cudaHostAlloc, or
+// cudaHostRegister with mapping), 16-byte aligned; nullptr for anything else.
+static void* mapped_host(const void* h) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, h) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return nullptr;
+  return aligned16(attr.devicePointer) ? attr.devicePointer : nullptr;
+}
+
 int32_t ep_dispatch_from_host(const ep_config* cfg, const ep_layout* layout,
                               const void* h_x, void* d_x, const float* d_topk_weights,
                               void* d_recv_x, float* d_recv_scale, float* d_recv_w,
@@ -326,10 +338,13 @@ int32_t ep_dispatch_from_host(const ep_config* cfg, const ep_layout* layout,
   if (!config_ok(cfg) || !layout_ptrs_ok(layout)) return EP_ERR_INVALID_ARG;
   const int T = layout->num_tokens;
   if (T < 0 || T > cfg->max_tokens) return EP_ERR_INVALID_ARG;
-  if (num_chunks < 1 || num_chunks > kMaxHostChunks) return EP_ERR_INVALID_ARG;
+  if (num_chunks < 0 || num_chunks > kMaxHostChunks) return EP_ERR_INVALID_ARG;
   if (d_recv_x == nullptr || !aligned16(d_recv_x)) return EP_ERR_INVALID_ARG;
-  if (T > 0 && (h_x == nullptr || d_x == nullptr || !aligned16(d_x)))
+  const bool direct = num_chunks == 0;
+  if (T > 0 && (h_x == nullptr || (!direct && (d_x == nullptr || !aligned16(d_x)))))
     return EP_ERR_INVALID_ARG;
+  const void* x_mapped = direct && T > 0 ? mapped_host(h_x) : nullptr;
+  if (direct && T > 0 && x_mapped == nullptr) return EP_ERR_INVALID_ARG;
   if (d_topk_weights != nullptr && !aligned16(d_topk_weights)) return EP_ERR_INVALID_ARG;
   if (d_recv_w != nullptr && !aligned16(d_recv_w)) return EP_ERR_INVALID_ARG;
   if (d_recv_w != nullptr && d_topk_weights == nullptr) return EP_ERR_INVALID_ARG;
@@ -337,7 +352,7 @@ int32_t ep_dispatch_from_host(const ep_config* cfg, const ep_layout* layout,
     return EP_ERR_INVALID_ARG;
   if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
   HostIo* io = nullptr;
-  if (host_io(&io) != cudaSuccess) return EP_ERR_CUDA;
+  if (!direct && host_io(&io) != cudaSuccess) return EP_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int K = cfg->num_topk;
   const int64_t row_bytes = int64_t(cfg->hidden) * 2;
@@ -357,8 +372,15 @@ int32_t ep_dispatch_from_host(const ep_config* cfg, const ep_layout* layout,
   base.err = layout->err;
   base.pdl = false;
   cudaError_t e = cudaSuccess;
-  const int tc = T > 0 ? chunk_tokens(T, num_chunks, row_bytes) : 0;
-  if (T > 0 && tc >= T) {
+  const int tc = T > 0 && !direct ? chunk_tokens(T, num_chunks, row_bytes) : 0;
+  if (direct && T > 0) {
+    // the kernel reads the rows where they are, once, over the host link
+    DispatchArgs a = base;
+    a.x = x_mapped;
+    a.T = T;
+    a.pdl = true;
+    e = launch_dispatch(a, s);
+  } else if (T > 0 && tc >= T) {
     // one chunk: the copy and the kernel in order on the caller's stream
     e = cudaMemcpyAsync(d_x, h_x, T * row_bytes, cudaMemcpyHostToDevice, s);
     DispatchArgs a = base;
@@ -404,14 +426,30 @@ int32_t ep_combine_to_host(const ep_config* cfg, const ep_layout* layout,
   if (!config_ok(cfg) || !layout_ptrs_ok(layout)) return EP_ERR_INVALID_ARG;
   const int T = layout->num_tokens;
   if (T < 0 || T > cfg->max_tokens) return EP_ERR_INVALID_ARG;
-  if (num_chunks < 1 || num_chunks > kMaxHostChunks) return EP_ERR_INVALID_ARG;
+  if (num_chunks < 0 || num_chunks > kMaxHostChunks) return EP_ERR_INVALID_ARG;
+  const bool direct = num_chunks == 0;
   if (T > 0) {
     if (d_expert_out == nullptr || !aligned16(d_expert_out)) return EP_ERR_INVALID_ARG;
-    if (d_y == nullptr || !aligned16(d_y) || h_y == nullptr) return EP_ERR_INVALID_ARG;
+    if (h_y == nullptr || (!direct && (d_y == nullptr || !aligned16(d_y))))
+      return EP_ERR_INVALID_ARG;
   }
   if (d_topk_weights != nullptr && !aligned16(d_topk_weights)) return EP_ERR_INVALID_ARG;
   if (T == 0) return EP_OK;
+  void* y_mapped = direct ? mapped_host(h_y) : nullptr;
+  if (direct && y_mapped == nullptr) return EP_ERR_INVALID_ARG;
   if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
+  if (direct) {
+    // the kernel writes the rows where they belong, once, over the host link
+    CombineArgs a;
+    a.expert_out = d_expert_out;
+    a.topk_weights = d_topk_weights;
+    a.slot_of = layout->slot_of;
+    a.T = T;
+    a.H = cfg->hidden;
+    a.K = cfg->num_topk;
+    a.y = y_mapped;
+    return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
+  }
   HostIo* io = nullptr;
   if (host_io(&io) != cudaSuccess) return EP_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -71,7 +71,9 @@ __device__ __forceinline__ int64_t scale_index(int64_t row, int blk, int nblk, i
 // loads), so 8 lanes cover one 128-channel block: exact amax by three
 // shuffles, scale = amax / 448, 16 E4M3 bytes written with one 16-byte store
 // per selected expert, and the block's scale by the group's first lane.
-template <bool kColMajor>
+// kWide: x is 32-byte aligned and each thread's 16 channels come in one
+// 256-bit load.
+template <bool kColMajor, bool kWide>
 __global__ void __launch_bounds__(1024)
     dispatch_fp8_kernel(const uint4* __restrict__ x,
                         const float* __restrict__ w,
@@ -101,8 +103,13 @@ __global__ void __launch_bounds__(1024)
     const bool active = u < n16;
     uint4 r0 = make_uint4(0, 0, 0, 0), r1 = r0;
     if (active) {
-      r0 = ld_stream_u4(x + int64_t(t) * nvec + 2 * u);
-      r1 = ld_stream_u4(x + int64_t(t) * nvec + 2 * u + 1);
+      const uint4* p = x + int64_t(t) * nvec + 2 * u;
+      if (kWide) {
+        ld_stream_u4x2(p, r0, r1);
+      } else {
+        r0 = ld_stream_u4(p);
+        r1 = ld_stream_u4(p + 1);
+      }
     }
     uint4 q;
     float scale;
@@ -282,7 +289,11 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
                      static_cast<const uint4*>(a.x), a.topk_weights, a.slot_of, nvec, a.K,
                      static_cast<uint4*>(a.recv_x), a.recv_w);
     } else if (a.x_q == nullptr) {
-      auto kern = a.scale_col_major ? dispatch_fp8_kernel<true> : dispatch_fp8_kernel<false>;
+      // rows start at multiples of 2H >= 256 bytes, so x's own alignment decides
+      const bool wide = (reinterpret_cast<uintptr_t>(a.x) & 31) == 0;
+      auto kern = a.scale_col_major
+                      ? (wide ? dispatch_fp8_kernel<true, true> : dispatch_fp8_kernel<true, false>)
+                      : (wide ? dispatch_fp8_kernel<false, true> : dispatch_fp8_kernel<false, false>);
       st = launch_ex(a.pdl, kern, dim3(a.T), dim3(threads_for(a.H / 16)), 0, stream,
                      static_cast<const uint4*>(a.x), a.topk_weights, a.slot_of, a.H,
                      a.K, a.scale_ld, static_cast<uint8_t*>(a.recv_x), a.recv_scale,

@@ -129,6 +129,16 @@ __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
   return v;
 }
 
+// Two adjacent 16-byte vectors in one 256-bit load (p 32-byte aligned): a
+// warp's request then covers each 32-byte sector once, which matters where
+// a sector read twice crosses the link twice (rows in host memory).
+__device__ __forceinline__ void ld_stream_u4x2(const void* p, uint4& a, uint4& b) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z),
+                 "=r"(b.w)
+               : "l"(p));
+}
+
 // ---- numerics ------------------------------------------------------------
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) {

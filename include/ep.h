@@ -392,7 +392,15 @@ EP_API int32_t ep_combine_ranks(const ep_config *cfg, const ep_layout *layout,
  * bound: a chunk carries at least 4 MiB of rows (T rows of 2H bytes split
  * into n = min(num_chunks, max(1, floor(2HT / 4 MiB))) chunks of
  * ceil(T / n) tokens, the last ragged); a single chunk is copied on `stream`
- * itself, with no copy stream involved. */
+ * itself, with no copy stream involved.
+ * num_chunks = 0 (direct): no copy and no staging buffer; the kernel reads
+ * (dispatch) or writes (combine) the host rows in place, each byte once over
+ * the host link, on `stream` alone.  The host buffer must then be page-locked
+ * memory the device can address (cudaHostAlloc, or cudaHostRegister with
+ * mapping) with a 16-byte aligned device address, else EP_ERR_INVALID_ARG;
+ * the staging pointer is not used and may be NULL.  On a link that the
+ * copy engine already saturates, this saves the staging traffic and the
+ * chunk hand-offs. */
 
 /* As ep_dispatch with x in host memory: h_x (host bf16 [T, H]) is copied
  * into d_x (device bf16 [T, H], a staging buffer the caller owns and that

@@ -108,8 +108,9 @@ def test_null_and_misaligned_pointers_rejected(ep):
     assert ep.ep_dispatch(cfg, lay, 0x30000, None, 0x40000, None, 0x50000, None) == ep.EP_ERR_INVALID_ARG
     cfg8 = ep.Config(16, 128, 2, 8, 2, 4, use_fp8_dispatch=True).c()
     assert ep.ep_dispatch(cfg8, lay, 0x30000, None, 0x40000, None, None, None) == ep.EP_ERR_INVALID_ARG
-    # host-buffer entry points: chunk count outside 1..64, missing host or
-    # staging buffer, misaligned staging buffer
+    # host-buffer entry points: chunk count outside 0..64, missing host or
+    # staging buffer, misaligned staging buffer; direct mode (0 chunks) on
+    # host memory that is not page-locked (a fake address)
     for chunks in (0, 65, -3):
         assert ep.ep_dispatch_from_host(cfg, lay, 0x60000, 0x30000, None, 0x40000, None, None,
                                         chunks, None) == ep.EP_ERR_INVALID_ARG

@@ -4,7 +4,8 @@ stream, each chunk's kernel waiting for its own copy.  The results must equal
 the device-buffer entry points bit for bit (which the parity suite holds to
 the oracle), for one chunk (on the caller's stream) and several (on the copy
 stream) with a ragged last chunk, FP8 rows and zero padding; one case is
-also compared with the oracle directly."""
+also compared with the oracle directly.  With 0 chunks (direct) the kernels
+read and write the pinned host rows in place, with no staging buffer."""
 
 import numpy as np
 import pytest
@@ -90,7 +91,9 @@ def _rows(L, cfg, zp):
 @pytest.mark.parametrize("name,chunks,zp", [
     ("ragged", 1, False), ("ragged", 8, True), ("fp8", 7, False), ("fp8", 4, True),
     ("few_tokens", 8, False), ("wide", 3, False), ("wide", 8, True), ("wide", 64, False),
-    ("wide_fp8", 5, False), ("wide_fp8", 8, True), ("prefill", 8, False)])
+    ("wide_fp8", 5, False), ("wide_fp8", 8, True), ("prefill", 8, False),
+    ("ragged", 0, False), ("fp8", 0, True), ("few_tokens", 0, False), ("wide", 0, True),
+    ("wide_fp8", 0, False), ("prefill", 0, False)])
 def test_host_buffers_equal_device_buffers(ep, name, chunks, zp):
     wl = CASES[name]
     inp, cfg, L, ref, got, y_ref, h_y = _run(ep, wl, chunks, zp)
@@ -101,8 +104,11 @@ def test_host_buffers_equal_device_buffers(ep, name, chunks, zp):
     if cfg.use_fp8_dispatch:
         assert torch.equal(gs[rows].view(torch.int32), rs[rows].view(torch.int32))
     assert torch.equal(gw[rows].view(torch.int32), rw[rows].view(torch.int32))
-    # the staging buffer holds x afterwards
-    assert np.array_equal(u16(staged), inp["x"])
+    if chunks:
+        # the staging buffer holds x afterwards
+        assert np.array_equal(u16(staged), inp["x"])
+    else:
+        assert staged is None
     assert np.array_equal(u16(h_y), u16(y_ref))
 
 
@@ -152,3 +158,53 @@ def test_empty_batch(ep):
     h_y, _ = ep.combine_to_host(cfg, L, recv, num_chunks=4)
     torch.cuda.synchronize()
     assert h_y.shape == (0, wl.hidden)
+
+
+def test_direct_mode_needs_page_locked_memory(ep):
+    wl = CASES["few_tokens"]
+    inp = workloads.make_inputs(wl, seed=0)
+    cfg = ep.Config(wl.num_tokens, wl.hidden, wl.num_topk, wl.num_experts, wl.num_ranks,
+                    wl.expert_alignment, False, False)
+    L = ep.get_layout(cfg, dev(inp["topk_idx"]), sync=True)
+    x_pageable = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16)
+    with pytest.raises(RuntimeError):
+        ep.dispatch_from_host(cfg, L, x_pageable, num_chunks=0)
+    recv, _, _ = ep.dispatch(cfg, L, x_pageable.cuda())
+    with pytest.raises(RuntimeError):
+        ep.combine_to_host(cfg, L, recv, h_y=torch.empty_like(x_pageable), num_chunks=0)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("where", ["device", "host"])
+def test_fp8_rows_at_16_byte_offset(ep, where):
+    """x 16 bytes past a 32-byte boundary takes two 16-byte loads per thread
+    instead of one 32-byte load: the same rows and scales either way, and
+    the oracle's."""
+    wl = CASES["fp8"]
+    inp = workloads.make_inputs(wl, seed=3)
+    T, H = wl.num_tokens, wl.hidden
+    cfg = ep.Config(T, H, wl.num_topk, wl.num_experts, wl.num_ranks, wl.expert_alignment,
+                    True, True)
+    L = ep.get_layout(cfg, dev(inp["topk_idx"]), sync=True)
+    w = dev(inp["topk_weights"])
+    flat = torch.empty(T * H + 8, dtype=torch.bfloat16)
+    flat = flat.pin_memory() if where == "host" else flat.cuda()
+    x_off = flat[8:].view(T, H)          # 16 bytes past the allocation's start
+    x_off.copy_(pinned_bf16(inp["x"]))
+    assert x_off.data_ptr() % 32 == 16
+    if where == "host":
+        gx, gs, gw, _ = ep.dispatch_from_host(cfg, L, x_off, topk_weights=w, num_chunks=0)
+    else:
+        gx, gs, gw = ep.dispatch(cfg, L, x_off, w)
+    rx, rs, rw = ep.dispatch(cfg, L, dev(inp["x"].view(np.int16)).view(torch.bfloat16), w)
+    torch.cuda.synchronize()
+    used = int(L.expert_start[-1].item())
+    assert torch.equal(gx[:used], rx[:used])
+    assert torch.equal(gs[:used].view(torch.int32), rs[:used].view(torch.int32))
+    ora = oracle.layout(inp["topk_idx"], wl.num_experts, wl.num_ranks, wl.expert_alignment,
+                        cap=cfg.capacity)
+    want_q, want_s, _ = oracle.dispatch_fp8(inp["x"], inp["topk_weights"], ora,
+                                            zero_padding=True)
+    assert np.array_equal(gx.cpu().numpy()[:used], want_q[:used])
+    assert np.array_equal(gs.cpu().numpy()[:used].view(np.uint32),
+                          want_s[:used].astype(np.float32).view(np.uint32))
