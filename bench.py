@@ -93,8 +93,8 @@ def parse_args():
                         "host memory in place (host-buffer entry points, 0 chunks); "
                         "chunked = the same entry points copying token chunks; copies = "
                         "whole-buffer copies on the stream around the device entry points; "
-                        "auto = direct for bf16 rows, else chunked when the rows span two "
-                        "4 MiB chunks, else copies")
+                        "auto = direct (copies with the combine epilogue or FP8 input "
+                        "options, which have device entry points only)")
     p.add_argument("--fused", action="store_true",
                    help="forward pass: layout and dispatch through ep_layout_and_dispatch "
                         "(one kernel for small inputs)")
@@ -734,13 +734,11 @@ def run_ours(args):
         idx_h = torch.from_numpy(inp["topk_idx"]).pin_memory()
         w_h = torch.from_numpy(inp["topk_weights"]).pin_memory()
         y_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-        ident = recv_x if not wl.use_fp8_dispatch else None
-        if ident is None:
-            # FP8 wire format: identity experts output the bf16 rows, which
-            # the bf16 dispatch of the same layout provides
-            ident = torch.empty((cap, H), dtype=torch.bfloat16, device=device)
-        bf_cfg = ep.Config(T, H, K, wl.num_experts, wl.num_ranks, wl.expert_alignment,
-                           False, False).c()
+        # Experts: identity for bf16 rows (combine reads the dispatched rows);
+        # for E4M3 rows, whose bf16 values no kernel of the path produces, the
+        # experts' output is the device leg's seeded expert-output buffer,
+        # already in HBM as a real expert's output would be.
+        ident = recv_x if not wl.use_fp8_dispatch else Y_d
         # The host-buffer entry points either let the kernels read x and write
         # y in pinned host memory in place (direct: each byte crosses the host
         # link once, no staging) or move the rows in token chunks overlapped
@@ -748,16 +746,12 @@ def run_ours(args):
         # least 4 MiB (below that, copying everything first and launching the
         # kernels back to back is faster).  The epilogue and FP8 input options
         # have device entry points only, so with those the rows are copied
-        # whole.  With FP8 rows the identity experts read the bf16 rows of a
-        # second, bf16 dispatch from the staged x, so x is staged.
+        # whole.
         transfer = args.e2e_transfer
         if epilogue or fp8_opts:
             transfer = "copies"
-        elif transfer == "direct" and wl.use_fp8_dispatch:
-            transfer = "chunked"
         elif transfer == "auto":
-            transfer = ("direct" if not wl.use_fp8_dispatch else
-                        "chunked" if T * H * 2 >= 2 * (4 << 20) else "copies")
+            transfer = "direct"
         host_io = transfer != "copies"
         chunks = 0 if transfer == "direct" else args.e2e_chunks
 
@@ -774,9 +768,6 @@ def run_ours(args):
                 assert st == 0, ep.ep_status_str(st)
             else:
                 dispatch(x_d)
-            if wl.use_fp8_dispatch:
-                st = ep.ep_dispatch(bf_cfg, L.c, p(x_d), None, p(ident), None, None, sptr)
-                assert st == 0
             if host_io:
                 st = ep.ep_combine_to_host(ccfg, L.c, p(ident), p(w_d),
                                            None if chunks == 0 else p(y_d), y_h.data_ptr(),
@@ -805,7 +796,9 @@ def run_ours(args):
         e2e = {"value": T * world / (e_ms / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": x_h.numel() * 2 + idx_h.numel() * 8 + w_h.numel() * 4,
                "d2h_bytes_per_step": y_h.numel() * 2, "ms_per_step": e_ms,
-               "experts": "identity (combine reads the dispatched bf16 rows)",
+               "experts": ("identity (combine reads the dispatched bf16 rows)"
+                           if not wl.use_fp8_dispatch else
+                           "combine reads the device leg's seeded expert-output buffer"),
                "transfer": ("ep_dispatch_from_host / ep_combine_to_host, direct (the "
                             "kernels read x and write y in pinned host memory)")
                            if transfer == "direct" else
