@@ -28,8 +28,9 @@
  *  - Pointers named d_* or documented "device" are CUDA device pointers; all
  *    buffers are allocated and owned by the CALLER.  The library never
  *    allocates or frees memory and keeps no pointer after a call returns.
- *    (The host-buffer entry points create one copy stream and a few events
- *    per device on first use, kept until exit.)
+ *    (The host-buffer entry points, when they copy in chunks, create one
+ *    copy stream and a few events per device on first use, kept until
+ *    exit.)
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Work is enqueued asynchronously on it; a call returns before
  *    the GPU has finished unless documented otherwise.
@@ -379,48 +380,52 @@ EP_API int32_t ep_combine_ranks(const ep_config *cfg, const ep_layout *layout,
 
 /* ---- Host buffers ---------------------------------------------------------
  * For callers whose token rows live in host memory (CPU-resident activations,
- * a serving loop that stages batches on the host).  The rows move in token
- * chunks on a copy stream the library owns, and each chunk's dispatch or
- * combine waits only for its own chunk's copy ("Deep Dive - DeepEP",
- * "EventOverlap: a stream contract": streams let data movement and compute
- * overlap; readiness is a stream dependency on an event, not a host wait).
- * Results equal ep_dispatch / ep_combine bit for bit.
- * The first call on a device creates that device's copy stream and events
- * (kept until exit); calls on one device share them, so their copies run in
- * call order.  Host buffers should be pinned (page-locked): pageable memory
- * works but its copies do not overlap.  num_chunks (1..64) is an upper
- * bound: a chunk carries at least 4 MiB of rows (T rows of 2H bytes split
- * into n = min(num_chunks, max(1, floor(2HT / 4 MiB))) chunks of
- * ceil(T / n) tokens, the last ragged); a single chunk is copied on `stream`
- * itself, with no copy stream involved.
- * num_chunks = 0 (direct): no copy and no staging buffer; the kernel reads
- * (dispatch) or writes (combine) the host rows in place, each byte once over
- * the host link, on `stream` alone.  The host buffer must then be page-locked
- * memory the device can address (cudaHostAlloc, or cudaHostRegister with
- * mapping) with a 16-byte aligned device address, else EP_ERR_INVALID_ARG;
- * the staging pointer is not used and may be NULL.  On a link that the
- * copy engine already saturates, this saves the staging traffic and the
- * chunk hand-offs. */
+ * a serving loop that stages batches on the host).  Results equal
+ * ep_dispatch / ep_combine bit for bit.  num_chunks selects how the rows
+ * cross the host link:
+ *  - 0 (direct): no copy and no staging buffer.  The kernel reads
+ *    (dispatch) or writes (combine) the host rows in place, each byte once
+ *    over the link, on `stream` alone.  The host buffer must be page-locked
+ *    memory the device can address (cudaHostAlloc, or cudaHostRegister with
+ *    mapping) whose device address is 16-byte aligned, else
+ *    EP_ERR_INVALID_ARG; the staging pointer is not used and may be NULL.
+ *    Where kernels reach the link's rate, this saves the staging traffic
+ *    and the chunk hand-offs.
+ *  - 1..64 (chunked): the rows move in token chunks on a copy stream the
+ *    library owns, and each chunk's dispatch or combine waits only for its
+ *    own chunk's copy ("Deep Dive - DeepEP", "EventOverlap: a stream
+ *    contract": streams let data movement and compute overlap; readiness is
+ *    a stream dependency on an event, not a host wait).  num_chunks is an
+ *    upper bound: a chunk carries at least 4 MiB of rows (T rows of 2H
+ *    bytes split into n = min(num_chunks, max(1, floor(2HT / 4 MiB)))
+ *    chunks of ceil(T / n) tokens, the last ragged); a single chunk is
+ *    copied on `stream` itself, with no copy stream involved.  The first
+ *    chunked call on a device creates that device's copy stream and events
+ *    (kept until exit); calls on one device share them, so their copies run
+ *    in call order.  Host buffers should be pinned (page-locked): pageable
+ *    memory works but its copies do not overlap. */
 
-/* As ep_dispatch with x in host memory: h_x (host bf16 [T, H]) is copied
- * into d_x (device bf16 [T, H], a staging buffer the caller owns and that
- * holds x afterwards) chunk by chunk, overlapped with the dispatch of the
- * chunks already copied.  The copies start once the work enqueued on
- * `stream` before this call is done (so d_x may still be read by it).
- * cfg->use_fp8_dispatch and cfg->zero_padding act as in ep_dispatch.
- * Returns EP_OK or an error. */
+/* As ep_dispatch with x in host memory (h_x: host bf16 [T, H]).  Direct
+ * (num_chunks = 0): the dispatch kernel reads h_x in place; d_x is unused.
+ * Chunked: h_x is copied into d_x (device bf16 [T, H], a staging buffer the
+ * caller owns and that holds x afterwards) chunk by chunk, overlapped with
+ * the dispatch of the chunks already copied; the copies start once the work
+ * enqueued on `stream` before this call is done (so d_x may still be read
+ * by it).  cfg->use_fp8_dispatch and cfg->zero_padding act as in
+ * ep_dispatch.  Returns EP_OK or an error. */
 EP_API int32_t ep_dispatch_from_host(const ep_config *cfg, const ep_layout *layout,
                                      const void *h_x, void *d_x,
                                      const float *d_topk_weights, void *d_recv_x,
                                      float *d_recv_scale, float *d_recv_w,
                                      int32_t num_chunks, void *stream);
 
-/* As ep_combine with y returned to host memory: each chunk of tokens is
- * combined into d_y (device bf16 [T, H], staging owned by the caller) and
- * then copied to h_y (host bf16 [T, H]) while later chunks combine.  Work
- * enqueued on `stream` after this call starts after the last copy, so a
- * synchronisation of `stream` makes h_y readable.  Returns EP_OK or an
- * error. */
+/* As ep_combine with y returned to host memory (h_y: host bf16 [T, H]).
+ * Direct (num_chunks = 0): the combine kernel writes h_y in place; d_y is
+ * unused.  Chunked: each chunk of tokens is combined into d_y (device bf16
+ * [T, H], staging owned by the caller) and then copied to h_y while later
+ * chunks combine.  Either way, work enqueued on `stream` after this call
+ * starts after the last row reached h_y, so a synchronisation of `stream`
+ * makes h_y readable.  Returns EP_OK or an error. */
 EP_API int32_t ep_combine_to_host(const ep_config *cfg, const ep_layout *layout,
                                   const void *d_expert_out, const float *d_topk_weights,
                                   void *d_y, void *h_y, int32_t num_chunks, void *stream);
