@@ -7,6 +7,8 @@ stream) with a ragged last chunk, FP8 rows and zero padding; one case is
 also compared with the oracle directly.  With 0 chunks (direct) the kernels
 read and write the pinned host rows in place, with no staging buffer."""
 
+import mmap
+
 import numpy as np
 import pytest
 import torch
@@ -208,3 +210,49 @@ def test_fp8_rows_at_16_byte_offset(ep, where):
     assert np.array_equal(gx.cpu().numpy()[:used], want_q[:used])
     assert np.array_equal(gs.cpu().numpy()[:used].view(np.uint32),
                           want_s[:used].astype(np.float32).view(np.uint32))
+
+
+def test_direct_mode_on_registered_memory(ep):
+    """Ordinary host arrays registered as page-locked and mapped
+    (cudaHostRegister) serve the direct mode as pinned allocations do."""
+    rt = torch.cuda.cudart()
+    if not hasattr(rt, "cudaHostRegister"):
+        pytest.skip("no cudaHostRegister binding in this torch")
+    wl = CASES["fp8"]
+    inp = workloads.make_inputs(wl, seed=4)
+    T, H = wl.num_tokens, wl.hidden
+    cfg = ep.Config(T, H, wl.num_topk, wl.num_experts, wl.num_ranks, wl.expert_alignment,
+                    True, False)
+    L = ep.get_layout(cfg, dev(inp["topk_idx"]), sync=True)
+    w = dev(inp["topk_weights"])
+    def page_aligned(shape):
+        # whole pages of their own, so that the two registrations do not share one
+        n = int(np.prod(shape)) * 2
+        return np.frombuffer(mmap.mmap(-1, (n + 4095) // 4096 * 4096), np.uint16,
+                             count=n // 2).reshape(shape)
+
+    x_np = page_aligned((T, H))
+    x_np[:] = inp["x"]
+    y_np = page_aligned((T, H))
+    mapped = 2  # cudaHostRegisterMapped
+    for a in (x_np, y_np):
+        assert int(rt.cudaHostRegister(a.ctypes.data, a.nbytes, mapped)) == 0
+    try:
+        x_h = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16)
+        y_h = torch.from_numpy(y_np.view(np.int16)).view(torch.bfloat16)
+        gx, gs, _, _ = ep.dispatch_from_host(cfg, L, x_h, topk_weights=w, num_chunks=0)
+        g = torch.Generator(device="cuda")
+        g.manual_seed(9)
+        Y = torch.randn((cfg.capacity, H), generator=g, device="cuda").to(torch.bfloat16)
+        ep.combine_to_host(cfg, L, Y, w, h_y=y_h, num_chunks=0)
+        rx, rs, _ = ep.dispatch(cfg, L, dev(inp["x"].view(np.int16)).view(torch.bfloat16), w)
+        y_ref = ep.combine(cfg, L, Y, w)
+        torch.cuda.synchronize()
+        rows = torch.from_numpy(_rows(L, cfg, False)).long().cuda()
+        assert torch.equal(gx[rows], rx[rows])
+        assert torch.equal(gs[rows].view(torch.int32), rs[rows].view(torch.int32))
+        assert np.array_equal(y_np, u16(y_ref))
+    finally:
+        torch.cuda.synchronize()
+        for a in (x_np, y_np):
+            rt.cudaHostUnregister(a.ctypes.data)
