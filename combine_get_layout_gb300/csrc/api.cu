@@ -71,7 +71,7 @@ static bool config_ok(const ep_config* c) {
   if (c->use_fp8_dispatch != 0 && c->use_fp8_dispatch != 1) return false;
   if (c->zero_padding != 0 && c->zero_padding != 1) return false;
   if (c->use_fp8_dispatch && c->hidden % 128 != 0) return false;
-  // bf16 rows are staged whole in shared memory (two stages at least)
+  // bf16 rows: up to the widest row the GPU parity cases cover
   if (!c->use_fp8_dispatch && c->hidden > 49152) return false;
   // all row indices fit in int32
   const int64_t cap = int64_t(c->max_tokens) * c->num_topk +
