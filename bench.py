@@ -396,6 +396,20 @@ def run_reference(args):
     return 0
 
 
+def e2e_transfer(requested: str, device_entry_points_only: bool) -> str:
+    """How the e2e leg moves x and y: "direct" (the host-buffer entry points
+    with 0 chunks: the kernels read and write pinned host memory in place),
+    "chunked" (the same entry points copying token chunks) or "copies"
+    (whole-buffer copies around the device entry points).  "auto" is
+    direct.  Options that only the device entry points offer (the combine
+    epilogue, the FP8 input options) force copies."""
+    if requested not in ("auto", "direct", "chunked", "copies"):
+        raise ValueError(f"unknown e2e transfer {requested!r}")
+    if device_entry_points_only:
+        return "copies"
+    return "direct" if requested == "auto" else requested
+
+
 def workload_config(wl, extra=None):
     d = {
         "workload": f"{wl.name}: T={wl.num_tokens} H={wl.hidden} E={wl.num_experts} "
@@ -747,11 +761,7 @@ def run_ours(args):
         # kernels back to back is faster).  The epilogue and FP8 input options
         # have device entry points only, so with those the rows are copied
         # whole.
-        transfer = args.e2e_transfer
-        if epilogue or fp8_opts:
-            transfer = "copies"
-        elif transfer == "auto":
-            transfer = "direct"
+        transfer = e2e_transfer(args.e2e_transfer, bool(epilogue or fp8_opts))
         host_io = transfer != "copies"
         chunks = 0 if transfer == "direct" else args.e2e_chunks
 
