@@ -31,6 +31,7 @@ EP_ERR_DUP_EXPERT = 3
 EP_ERR_CAPACITY = 4
 EP_ERR_CUDA = 5
 EP_ERR_TIMEOUT = 6
+EP_ERR_TIMEOUT_PENDING = 7
 
 # The entry points include/ep.h declares (kept in sync by a test).
 ABI_SYMBOLS = (
@@ -54,6 +55,7 @@ ABI_SYMBOLS = (
     "ep_combine_to_host",
     "ep_check_error",
     "ep_selftest_wait_timeout",
+    "ep_selftest_layout_timeout",
     "ep_selftest_fp8_quotient",
     "ep_last_cuda_error",
     "ep_get_layout_noalloc",
@@ -146,6 +148,8 @@ def _load():
     L.ep_selftest_fp8_quotient.argtypes = [vp, vp, vp]
     L.ep_selftest_wait_timeout.restype = i32
     L.ep_selftest_wait_timeout.argtypes = [i64, vp, vp]
+    L.ep_selftest_layout_timeout.restype = i32
+    L.ep_selftest_layout_timeout.argtypes = [P(EpConfig), i32, vp, P(EpLayout), i32, i64, vp]
     L.ep_get_layout_noalloc.restype = i32
     L.ep_get_layout_noalloc.argtypes = [P(EpConfig), i32, vp, P(EpLayout), vp, vp]
     L.ep_last_cuda_error.restype = i32
@@ -280,6 +284,13 @@ def ep_selftest_fp8_quotient(d_counts, d_first, stream) -> int:
 
 def ep_selftest_wait_timeout(timeout_ns, d_err, stream) -> int:
     return int(_lib.ep_selftest_wait_timeout(int(timeout_ns), d_err, stream))
+
+
+def ep_selftest_layout_timeout(cfg, num_tokens, d_topk_idx, layout, stall_tile, timeout_ns,
+                               stream) -> int:
+    return int(_lib.ep_selftest_layout_timeout(ctypes.byref(cfg), num_tokens, d_topk_idx,
+                                               ctypes.byref(layout), int(stall_tile),
+                                               int(timeout_ns), stream))
 
 
 def ep_get_layout_noalloc(cfg, num_tokens, d_topk_idx, layout, h_expert_count,

@@ -92,6 +92,7 @@ static int32_t cuda_status(cudaError_t e) {
 static int32_t status_from_bits(int32_t bits) {
   if (bits & ERRBIT_EXPERT_RANGE) return EP_ERR_EXPERT_RANGE;
   if (bits & ERRBIT_DUP_EXPERT) return EP_ERR_DUP_EXPERT;
+  if (bits & ERRBIT_TIMEOUT_PENDING) return EP_ERR_TIMEOUT_PENDING;
   if (bits & ERRBIT_TIMEOUT) return EP_ERR_TIMEOUT;
   return EP_OK;
 }
@@ -783,6 +784,31 @@ int32_t ep_selftest_wait_timeout(int64_t timeout_ns, int32_t* d_err, void* strea
   return status_from_bits(bits);
 }
 
+int32_t ep_selftest_layout_timeout(const ep_config* cfg, int32_t num_tokens,
+                                   const int64_t* d_topk_idx, ep_layout* layout,
+                                   int32_t stall_tile, int64_t timeout_ns, void* stream) {
+  LayoutArgs a;
+  const int32_t v = layout_args(cfg, num_tokens, d_topk_idx, layout, &a);
+  if (v != EP_OK) return v;
+  if (timeout_ns < 1000 || timeout_ns > 1000000000) return EP_ERR_INVALID_ARG;
+  // the two-launch layout only (the one-launch layout has no waits)
+  if (num_tokens == 0 || layout_is_small(num_tokens, a.K, a.E)) return EP_ERR_INVALID_ARG;
+  if (stall_tile < 0 || stall_tile >= assign_grid(a.geom.num_tiles, a.E))
+    return EP_ERR_INVALID_ARG;
+  if (ensure_prepared() != cudaSuccess) return EP_ERR_CUDA;
+  a.stall_tile = stall_tile;
+  a.wait_ns = uint64_t(timeout_ns);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_layout(a, s);
+  layout->num_tokens = num_tokens;
+  int32_t bits = 0;
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&bits, layout->err, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (note_cuda(e) != cudaSuccess) return EP_ERR_CUDA;
+  return status_from_bits(bits);
+}
+
 int32_t ep_last_cuda_error(void) {
   const cudaError_t e = g_last_cuda_error;
   g_last_cuda_error = cudaSuccess;
@@ -798,6 +824,7 @@ const char* ep_status_str(int32_t status) {
     case EP_ERR_CAPACITY: return "EP_ERR_CAPACITY";
     case EP_ERR_CUDA: return "EP_ERR_CUDA";
     case EP_ERR_TIMEOUT: return "EP_ERR_TIMEOUT";
+    case EP_ERR_TIMEOUT_PENDING: return "EP_ERR_TIMEOUT_PENDING";
     default: return "EP_ERR_UNKNOWN";
   }
 }

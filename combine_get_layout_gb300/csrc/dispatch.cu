@@ -214,33 +214,31 @@ cudaError_t launch_wait_selftest(uint64_t timeout_ns, int32_t* err, cudaStream_t
 
 cudaError_t prepare_dispatch_kernels() { return cudaSuccess; }
 
-// Exhaustive check of scaled_quotient: block b takes the block maximum
-// amax = the positive finite bf16 with bits b + 1, every thread a share of
-// the 65536 bf16 values x with |x| <= amax; counts[0] += pairs whose E4M3
-// codes differ from those of __fdiv_rn, counts[1] += pairs whose fp32
-// quotients differ, counts[2] += those of them whose IEEE quotient is a
-// normal fp32 number; *first = (amax bits << 16 | x bits) of one code
-// mismatch.
+// Exhaustive check of the FP8 dispatch's block quotient (BlockQuotient):
+// block b takes the block maximum amax = the positive bf16 with bits b + 1
+// (every finite one, then +inf), every thread a share of the 65536 bf16
+// values x with |x| <= amax; counts[0] += pairs whose E4M3 codes differ from
+// those of __fdiv_rn, counts[1] += pairs whose fp32 quotients differ,
+// counts[2] += those of them whose IEEE quotient is a normal fp32 number;
+// *first = (amax bits << 16 | x bits) of one code mismatch.
 __global__ void __launch_bounds__(256)
     fp8_quotient_selftest_kernel(unsigned long long* __restrict__ counts,
                                  int32_t* __restrict__ first) {
   const uint32_t ab = blockIdx.x + 1;
   const float amax = __uint_as_float(ab << 16);
   const float s = __fdiv_rn(amax, 448.0f);
+  const BlockQuotient div(s);
   unsigned long long bad_code = 0, bad_f32 = 0, bad_normal = 0;
-  if (s >= kFastScaleMin) {
-    const float y = __frcp_rn(s);
-    for (uint32_t xb = threadIdx.x; xb < 65536u; xb += blockDim.x) {
-      const float x = __uint_as_float(xb << 16);
-      if (!(fabsf(x) <= amax)) continue;  // also NaN
-      const float qa = scaled_quotient(x, s, y), qb = __fdiv_rn(x, s);
-      const bool differ = __float_as_uint(qa) != __float_as_uint(qb);
-      bad_f32 += differ;
-      bad_normal += differ && fabsf(qb) >= 0x1p-126f;
-      if (pack_e4m3x2(qa, 0.0f) != pack_e4m3x2(qb, 0.0f)) {
-        ++bad_code;
-        atomicCAS(first, -1, int32_t((ab << 16) | xb));
-      }
+  for (uint32_t xb = threadIdx.x; xb < 65536u; xb += blockDim.x) {
+    const float x = __uint_as_float(xb << 16);
+    if (!(fabsf(x) <= amax)) continue;  // also NaN
+    const float qa = div(x), qb = __fdiv_rn(x, s);
+    const bool differ = __float_as_uint(qa) != __float_as_uint(qb);
+    bad_f32 += differ;
+    bad_normal += differ && fabsf(qb) >= 0x1p-126f;
+    if (pack_e4m3x2(qa, 0.0f) != pack_e4m3x2(qb, 0.0f)) {
+      ++bad_code;
+      atomicCAS(first, -1, int32_t((ab << 16) | xb));
     }
   }
 #pragma unroll
@@ -261,8 +259,8 @@ cudaError_t launch_fp8_quotient_selftest(unsigned long long* counts, int32_t* fi
   cudaError_t st = cudaMemsetAsync(counts, 0, 3 * sizeof(unsigned long long), stream);
   if (st == cudaSuccess) st = cudaMemsetAsync(first, 0xff, sizeof(int32_t), stream);
   if (st != cudaSuccess) return st;
-  // positive finite bf16: bits 0x0001 .. 0x7f7f
-  fp8_quotient_selftest_kernel<<<0x7f7f, 256, 0, stream>>>(counts, first);
+  // positive bf16 block maxima: bits 0x0001 .. 0x7f7f (finite), 0x7f80 (+inf)
+  fp8_quotient_selftest_kernel<<<0x7f80, 256, 0, stream>>>(counts, first);
   return cudaGetLastError();
 }
 

@@ -13,6 +13,9 @@ enum : int32_t {
   ERRBIT_EXPERT_RANGE = 1,
   ERRBIT_DUP_EXPERT = 2,
   ERRBIT_TIMEOUT = 4,
+  // a wait gave up and the bulk copies its CTA had issued were still not
+  // complete when it returned (they may land in shared memory after it)
+  ERRBIT_TIMEOUT_PENDING = 8,
 };
 
 // Default limit of one on-chip wait.  Far above any legitimate latency; a

@@ -70,9 +70,16 @@ struct LayoutArgs {
   uint8_t* is_token_in_rank;
   // optional rank rows (all set or all null)
   int32_t *rank_row_start = nullptr, *rank_slot_of = nullptr, *rank_src = nullptr;
+  // self-test of the assign kernel's bounded wait: the CTA numbered
+  // stall_tile issues no copy and waits wait_ns for it (-1: none)
+  int stall_tile = -1;
+  uint64_t wait_ns = 1000ull * 1000ull * 1000ull;
 };
 
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream);
+
+// CTAs of the assign kernel for a layout of `tiles` tiles over E experts.
+int assign_grid(int tiles, int E);
 
 // Dispatch work handed to the one-launch layout (layout_small_kernel).
 struct SmallDispatch {

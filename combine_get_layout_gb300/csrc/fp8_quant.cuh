@@ -7,8 +7,8 @@
 
 namespace ep {
 
-// x / s for a block scale s >= kFastScaleMin and |x| <= 448 s, given
-// y = RN(1/s): q0 = x * y, then one correction with the exact residual
+// x / s for a block scale s in [kFastScaleMin, FLT_MAX] and |x| <= 448 s,
+// given y = RN(1/s): q0 = x * y, then one correction with the exact residual
 // r = x - q0 * s (one FMA), after Markstein's FMA-based division
 // (P. Markstein, "IA-64 and Elementary Functions", 2000).  The reciprocal
 // is taken once per block.  The quotient can differ from the IEEE one in
@@ -24,6 +24,23 @@ __device__ __forceinline__ float scaled_quotient(float x, float s, float y) {
   // s > 0: the quotient has x's sign (the correction would turn -0 into +0)
   return copysignf(fmaf(r, y, q0), x);
 }
+
+// The quotient x / s of one block, by the fast form where it holds and by
+// IEEE division elsewhere: below kFastScaleMin 1/s would overflow, and an
+// infinite scale (a block holding +-inf) would make the residual inf - inf;
+// there the division gives +-0 for finite x and NaN for +-inf, as the
+// definition does.
+struct BlockQuotient {
+  float s, y;
+  bool fast;
+  __device__ __forceinline__ explicit BlockQuotient(float scale)
+      : s(scale), y(0.0f), fast(scale >= kFastScaleMin && scale <= 0x1.fffffep127f) {
+    if (fast) y = __frcp_rn(scale);
+  }
+  __device__ __forceinline__ float operator()(float x) const {
+    return fast ? scaled_quotient(x, s, y) : __fdiv_rn(x, s);
+  }
+};
 
 // One 16-channel group of a row (two 16-byte bf16 vectors r0, r1; zeros for
 // a lane past the row): 8 aligned lanes hold one 128-channel block.  The
@@ -46,14 +63,14 @@ __device__ __forceinline__ void quantize_group16(uint4 r0, uint4 r1, uint4* q, f
   *scale = 0.0f;
   if (amax != 0.0f) {
     const float s = __fdiv_rn(amax, 448.0f);
+    const BlockQuotient div(s);
     uint32_t p[8];
-    if (s >= kFastScaleMin) {
-      const float y = __frcp_rn(s);
+    if (div.fast) {
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        p[j] = pack_e4m3x2(scaled_quotient(f[2 * j], s, y),
-                           scaled_quotient(f[2 * j + 1], s, y));
-    } else {  // 1 / s would overflow: divide
+        p[j] = pack_e4m3x2(scaled_quotient(f[2 * j], s, div.y),
+                           scaled_quotient(f[2 * j + 1], s, div.y));
+    } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         p[j] = pack_e4m3x2(__fdiv_rn(f[2 * j], s), __fdiv_rn(f[2 * j + 1], s));

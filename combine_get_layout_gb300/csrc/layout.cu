@@ -169,7 +169,8 @@ __global__ void __launch_bounds__(kLayoutThreads)
                         int E, int R, int tile_tokens,
                         int32_t* __restrict__ tile_counts,
                         int32_t* __restrict__ tile_err,
-                        uint8_t* __restrict__ is_token_in_rank) {
+                        uint8_t* __restrict__ is_token_in_rank,
+                        int32_t* __restrict__ err) {
   extern __shared__ int32_t smem_i32[];
   __shared__ int32_t s_err;
   const int Wc = count_row_width(E, R);
@@ -183,17 +184,21 @@ __global__ void __launch_bounds__(kLayoutThreads)
   pdl_wait();
 
   const int tile = blockIdx.x;
+  // The call's error word starts at zero here; the assign kernel (which
+  // waits for this grid) only ORs bits into it, so a timeout one of its
+  // CTAs records is never overwritten.
+  if (tile == 0 && tid == 0) *err = 0;
   const int t0 = tile * tile_tokens;
   const int nt = min(tile_tokens, T - t0);
   const int64_t* src = topk_idx + int64_t(t0) * K;
-  int err = 0;
+  int bits = 0;
   // Warps take token-aligned spans: expert histogram (shared adds),
   // duplicate experts, destination ranks.
   const int span = (nt + kLayoutWarps - 1) / kLayoutWarps;
   const int tb = min(nt, warp * span), te = min(nt, tb + span);
   survey_span(src, tb, te, K, E, R, lane, hist, is_token_in_rank + int64_t(t0) * R, rcnt,
-              err);
-  if (err) atomicOr(&s_err, err);
+              bits);
+  if (bits) atomicOr(&s_err, bits);
   __syncthreads();
 
   for (int e = tid; e < Wc; e += blockDim.x)
@@ -296,7 +301,8 @@ __global__ void __launch_bounds__(kLayoutThreads)
                          int32_t* __restrict__ rank_row_start,
                          int32_t* __restrict__ rank_slot_of,
                          int32_t* __restrict__ rank_src,
-                         int32_t* __restrict__ err) {
+                         int32_t* __restrict__ err, int stall_tile,
+                         uint64_t wait_ns) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int Epad = padded_experts(E);
   const int Wc = count_row_width(E, R);
@@ -334,16 +340,22 @@ __global__ void __launch_bounds__(kLayoutThreads)
   __syncthreads();
   pdl_wait();
 
-  // Stream the tile-count matrix through two shared-memory buffers.
+  // Stream the tile-count matrix through two shared-memory buffers.  The
+  // CTA numbered stall_tile (a self-test; -1 otherwise) issues no copy, so
+  // its first wait runs out.
   const int rows = L.chunk_rows;
   const int nchunks = num_tiles > 0 ? (num_tiles + rows - 1) / rows : 0;
+  const bool stall = tile == stall_tile;
+  int issued = 0;   // chunks whose copy thread 0 has issued
   auto issue = [&](int ch) {
+    if (stall) return;
     const int r0 = ch * rows;
     const int n = min(rows, num_tiles - r0);
     const uint32_t bytes = uint32_t(n) * uint32_t(Wc) * 4u;
     mbar_arrive_expect_tx(&bar[ch & 1], bytes);
     bulk_load(ring + (ch & 1) * rows * Wc, tile_counts + int64_t(r0) * Wc,
               bytes, &bar[ch & 1]);
+    issued = ch + 1;
   };
   if (tid == 0) {
     if (nchunks > 0) issue(0);
@@ -378,7 +390,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
   // Per expert: rows of earlier tiles (this tile's base) and of all tiles.
   int failed = -1;
   for (int ch = 0; ch < nchunks; ++ch) {
-    if (tid == 0) s_scr[32] = mbar_wait(&bar[ch & 1], (ch >> 1) & 1, kWaitTimeoutNs);
+    if (tid == 0) s_scr[32] = mbar_wait(&bar[ch & 1], (ch >> 1) & 1, wait_ns);
     __syncthreads();
     if (!s_scr[32]) {
       failed = ch;
@@ -433,11 +445,15 @@ __global__ void __launch_bounds__(kLayoutThreads)
   }
   if (failed >= 0) {
     // A copy did not land in time: report, wait (bounded) for the copies
-    // still in flight -- chunks `failed` and `failed + 1` -- and leave.
+    // this CTA issued that are still in flight -- chunks [failed, issued) --
+    // and leave without writing rows.  Should one of those waits give up
+    // too, the copy may still land in this SM's shared memory after the CTA
+    // ends; that is reported as a bit of its own.
     if (tid == 0) {
       record_error(err, ERRBIT_TIMEOUT);
-      for (int ch = failed; ch < nchunks && ch <= failed + 1; ++ch)
-        (void)mbar_wait(&bar[ch & 1], (ch >> 1) & 1, kWaitTimeoutNs);
+      for (int ch = failed; ch < issued; ++ch)
+        if (!mbar_wait(&bar[ch & 1], (ch >> 1) & 1, kWaitTimeoutNs))
+          record_error(err, ERRBIT_TIMEOUT_PENDING);
     }
     return;
   }
@@ -517,7 +533,16 @@ __global__ void __launch_bounds__(kLayoutThreads)
     __syncthreads();
     if (bits) atomicOr(&s_scr[33], bits);
     __syncthreads();
-    if (tid == 0) *err = s_scr[33];
+    // OR-ed in: the count kernel cleared the word, and another CTA may
+    // already have recorded a timeout.  With no tokens there was no count
+    // kernel and this is the grid's only CTA, so it stores.
+    if (tid == 0) {
+      if (num_tiles > 0) {
+        if (s_scr[33]) atomicOr(err, s_scr[33]);
+      } else {
+        *err = s_scr[33];
+      }
+    }
   }
 
   // Tokens per destination rank (totals of the rank columns).
@@ -753,6 +778,8 @@ __global__ void __launch_bounds__(kLayoutThreads)
     }
     if (tid == 0) {
       expert_start[E] = s_start[E];
+      // this launch has no waits and no other writer of the word: the store
+      // both clears it and publishes the call's routing errors
       *err = s_scr[33];
     }
     for (int r = tid; r <= R; r += blockDim.x) rank_start[r] = s_start[r * Eg];
@@ -865,6 +892,13 @@ bool layout_is_small(int64_t T, int K, int E) {
   return T * K <= kSmallLayoutPairs && E <= kSmallLayoutMaxExperts;
 }
 
+int assign_grid(int tiles, int E) {
+  int grid = tiles > 0 ? tiles : 1;
+  const int pad_blocks = E < kLayoutMaxTiles ? E : kLayoutMaxTiles;
+  if (tiles > 0 && grid < pad_blocks) grid = pad_blocks;
+  return grid;
+}
+
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
   if (layout_is_small(a.T, a.K, a.E)) {
     return launch_pdl(layout_small_kernel<0>, dim3(kSmallLayoutCtas), dim3(kLayoutThreads),
@@ -880,22 +914,20 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
     st = launch_pdl(layout_count_kernel, dim3(tiles), dim3(kLayoutThreads),
                     count_smem(a.E, a.R, a.K), stream, a.topk_idx, a.T, a.K,
                     a.E, a.R, tt, a.ws.tile_counts, a.ws.tile_err,
-                    a.is_token_in_rank);
+                    a.is_token_in_rank, a.err);
     if (st != cudaSuccess) return st;
   }
   // With no tokens there are no tiles: one CTA still publishes the empty
   // layout (zero counts and offsets).
   const AssignSmem sm = assign_smem(a.E, a.R, tiles);
-  int grid = tiles > 0 ? tiles : 1;
-  const int pad_blocks = a.E < kLayoutMaxTiles ? a.E : kLayoutMaxTiles;
-  if (tiles > 0 && grid < pad_blocks) grid = pad_blocks;
+  const int grid = assign_grid(tiles, a.E);
   return launch_pdl(layout_assign_kernel, dim3(grid), dim3(kLayoutThreads),
                     sm.bytes, stream, a.topk_idx, a.T, a.K, a.E, a.R, a.A, tt,
                     tiles, a.ws.tile_counts, a.ws.tile_err,
                     static_cast<const uint8_t*>(a.is_token_in_rank), a.expert_count,
                     a.expert_start, a.expert_end, a.rank_start, a.tokens_per_rank,
                     a.slot_of, a.src_info, a.rank_row_start, a.rank_slot_of,
-                    a.rank_src, a.err);
+                    a.rank_src, a.err, a.stall_tile, a.wait_ns);
 }
 
 // Rows of the pairs one CTA of the one-launch layout owns, at most.

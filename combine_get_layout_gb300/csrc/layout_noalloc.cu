@@ -63,7 +63,10 @@ extern "C" int32_t ep_get_layout_noalloc(const ep_config* cfg, int32_t num_token
   if (cfg == nullptr || layout == nullptr) return EP_ERR_INVALID_ARG;
   const int64_t need = ep_layout_workspace_bytes(cfg);
   if (need < 0) return EP_ERR_INVALID_ARG;
-  if (need > static_cast<int64_t>(ep::kNoAllocScratchBytes)) return EP_ERR_CAPACITY;
+  // only the two-launch layout uses the scratch
+  if (need > static_cast<int64_t>(ep::kNoAllocScratchBytes) &&
+      !ep::layout_is_small(num_tokens, cfg->num_topk, cfg->num_experts))
+    return EP_ERR_CAPACITY;
   void* scratch = nullptr;
   const int32_t st = ep::scratch_address(&scratch);
   if (st != EP_OK) return st;

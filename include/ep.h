@@ -69,7 +69,12 @@ enum {
   EP_ERR_DUP_EXPERT = 3,    /* an expert selected twice by one token       */
   EP_ERR_CAPACITY = 4,      /* a buffer or built-in scratch is too small   */
   EP_ERR_CUDA = 5,          /* a CUDA runtime call failed                  */
-  EP_ERR_TIMEOUT = 6        /* a bounded on-chip wait gave up (no hang)    */
+  EP_ERR_TIMEOUT = 6,       /* a bounded on-chip wait gave up (no hang)    */
+  EP_ERR_TIMEOUT_PENDING = 7 /* as EP_ERR_TIMEOUT, and a bulk copy the
+                                waiting CTA had issued was still not done
+                                when it returned: it may still write that
+                                SM's shared memory, so treat the CUDA
+                                context as unreliable                     */
 };
 
 /* Problem statement, as in the pages' buffer constructor: max tokens,
@@ -225,11 +230,13 @@ EP_API int32_t ep_layout_and_dispatch(const ep_config *cfg, int32_t num_tokens,
  * Same arguments and results as ep_get_layout, except that
  * layout->workspace is ignored (it may be NULL): the per-tile scratch lives
  * in a 1 MiB array in the library's own device memory, which every GPU that
- * loads the library holds until the process exits.  Configurations whose
- * ep_layout_workspace_bytes exceeds 1 MiB (152 * 4 * (E rounded up to 4 +
- * R rounded up to 4) + 608 bytes) are rejected with EP_ERR_CAPACITY before
- * anything is launched.  Nothing is allocated or freed, by this call or by
- * any routine it calls.
+ * loads the library holds until the process exits.  Only layouts of more
+ * than 4096 (t, k) pairs (num_tokens * K > 4096, which take two launches)
+ * use scratch; of those, configurations whose ep_layout_workspace_bytes
+ * exceeds 1 MiB (152 * 4 * (E rounded up to 4 + R rounded up to 4) + 608
+ * bytes) are rejected with EP_ERR_CAPACITY before anything is launched.
+ * Smaller layouts are accepted whatever E and R.  Nothing is allocated or
+ * freed, by this call or by any routine it calls.
  *
  * The first call on each device looks up the array's device address (with
  * that device current) and caches it; make that first call before any
@@ -432,8 +439,12 @@ EP_API int32_t ep_combine_to_host(const ep_config *cfg, const ep_layout *layout,
                                   void *d_y, void *h_y, int32_t num_chunks, void *stream);
 
 /* Synchronises `stream` and returns the status recorded in the layout's
- * device error word (EP_OK if none): routing errors found by ep_get_layout,
- * and EP_ERR_TIMEOUT if a bounded on-chip wait of a later call gave up. */
+ * device error word by the last layout call (EP_OK if none): routing errors,
+ * else EP_ERR_TIMEOUT_PENDING or EP_ERR_TIMEOUT if one of its bounded
+ * on-chip waits gave up.  Each layout call clears the word before its
+ * kernels record anything, so a status never carries over from an earlier
+ * call.  After a timeout, part of the layout was not written: do not use it
+ * for dispatch or combine. */
 EP_API int32_t ep_check_error(const ep_layout *layout, void *stream);
 
 /* Self-test of the FP8 dispatch arithmetic ("Deep Dive - DeepEP",
@@ -441,10 +452,11 @@ EP_API int32_t ep_check_error(const ep_layout *layout, void *stream);
  * 128 values; the scale here is amax / 448 and each value is quantised from
  * x / scale rounded to nearest).  The dispatch forms x / scale as a product
  * with the block's reciprocal plus one fused multiply-add correction, which
- * may differ from the IEEE quotient in its last bit; this runs it for every
- * positive finite bf16 block maximum and every bf16 value x with
- * |x| <= amax (about 2^31 pairs: the whole input domain) beside the IEEE
- * division and compares the E4M3 codes.
+ * may differ from the IEEE quotient in its last bit (blocks whose scale is
+ * below 2^-100 or infinite divide); this runs the dispatch's quotient for
+ * every positive bf16 block maximum, finite or +inf, and every bf16 value x
+ * with |x| <= amax (about 2^31 pairs: the whole non-NaN input domain)
+ * beside the IEEE division and compares the E4M3 codes.
  * d_counts: device uint64 [3], 16-byte aligned: [0] = pairs whose E4M3
  * codes differ (0: the dispatch's codes equal those of the IEEE division),
  * [1] = pairs whose fp32 quotients differ, [2] = those of them whose IEEE
@@ -464,6 +476,24 @@ EP_API int32_t ep_selftest_fp8_quotient(uint64_t *d_counts, int32_t *d_first,
  * timeout_ns must be in [1000, 10^9]. */
 EP_API int32_t ep_selftest_wait_timeout(int64_t timeout_ns, int32_t *d_err,
                                         void *stream);
+
+/* Self-test of the layout's own bounded wait ("Deep Dive - DeepEP",
+ * "Benchmark and failure-mode checklist": a timeout is a failure boundary,
+ * reported, never a hang).  Runs the two-launch layout of ep_get_layout
+ * (same arguments; num_tokens * K above 4096 or E above 2048, so that the
+ * layout takes two launches) except that CTA `stall_tile` of its second
+ * kernel issues no copy of the per-tile counts and waits for it with a
+ * limit of timeout_ns nanoseconds (in [1000, 10^9]).  That wait gives up,
+ * the CTA records EP_ERR_TIMEOUT in the layout's error word and returns
+ * without writing its rows; the other CTAs finish.  stall_tile must be in
+ * [0, CTAs of that kernel): 0 .. max(tiles, min(E, 152)) - 1, where tiles
+ * is the number of token tiles (at most 152).  Synchronises `stream` and
+ * returns the recorded status (EP_ERR_TIMEOUT when the mechanism works);
+ * the layout it leaves is incomplete and must not be used. */
+EP_API int32_t ep_selftest_layout_timeout(const ep_config *cfg, int32_t num_tokens,
+                                          const int64_t *d_topk_idx, ep_layout *layout,
+                                          int32_t stall_tile, int64_t timeout_ns,
+                                          void *stream);
 
 /* The cudaError_t of the last CUDA runtime call of this library that failed
  * in the calling thread (0 if none since the previous query); reading it

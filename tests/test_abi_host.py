@@ -149,7 +149,28 @@ def test_null_and_misaligned_pointers_rejected(ep):
                                      0x50000, None) == ep.EP_ERR_INVALID_ARG  # recv_w, no w
 
 
+@pytest.mark.skipif(_has_gpu(), reason="uses fake device addresses: host-only check")
+def test_layout_timeout_selftest_arguments_checked(ep):
+    """ep_selftest_layout_timeout validates its arguments before launching:
+    the two-launch layout only, a stall CTA inside the assign grid, a limit in
+    [1 us, 1 s]."""
+    fake = [0x10000 + 0x100 * i for i in range(10)]
+    lay = ep.EpLayout(*fake, None, None, None, 0, 0)
+    big = ep.Config(4096, 128, 2, 8, 2, 4).c()       # 8192 pairs: 32 tiles, 32 CTAs
+    small = ep.Config(4096, 128, 2, 8, 2, 4).c()
+    call = lambda cfg, T, tile, ns: ep.ep_selftest_layout_timeout(cfg, T, 0x20000, lay, tile,
+                                                                  ns, None)
+    assert call(small, 2048, 0, 10_000) == ep.EP_ERR_INVALID_ARG   # 4096 pairs: one launch
+    assert call(big, 0, 0, 10_000) == ep.EP_ERR_INVALID_ARG        # no tokens
+    assert call(big, 4096, -1, 10_000) == ep.EP_ERR_INVALID_ARG
+    assert call(big, 4096, 32, 10_000) == ep.EP_ERR_INVALID_ARG    # past the grid
+    assert call(big, 4096, 0, 999) == ep.EP_ERR_INVALID_ARG
+    assert call(big, 4096, 0, 10**9 + 1) == ep.EP_ERR_INVALID_ARG
+    assert call(big, 4097, 0, 10_000) == ep.EP_ERR_INVALID_ARG     # > max_tokens
+
+
 def test_status_strings(ep):
     assert ep.ep_status_str(0) == "EP_OK"
     assert ep.ep_status_str(ep.EP_ERR_TIMEOUT) == "EP_ERR_TIMEOUT"
+    assert ep.ep_status_str(ep.EP_ERR_TIMEOUT_PENDING) == "EP_ERR_TIMEOUT_PENDING"
     assert ep.ep_status_str(99) == "EP_ERR_UNKNOWN"

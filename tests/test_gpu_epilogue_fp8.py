@@ -160,12 +160,14 @@ def test_fp8_dispatch_argument_checks(ep):
 
 
 def test_fp8_quotient_exhaustive(ep):
-    """The dispatch's x / scale (reciprocal product plus one FMA correction)
-    gives the E4M3 code of the IEEE division for every bf16 block maximum and
-    every bf16 value in its block (about 2^31 pairs: the whole input domain,
-    so the FP8 payloads equal the oracle's for any input).  The fp32
-    quotients themselves may differ in the last bit; those counts are
-    reported, not asserted."""
+    """The dispatch's x / scale (reciprocal product plus one FMA correction
+    where the scale allows it, IEEE division where it does not) gives the
+    E4M3 code of the IEEE division for every positive bf16 block maximum,
+    finite or +inf, and every bf16 value in its block (about 2^31 pairs: the
+    whole non-NaN input domain, so the FP8 payloads equal the oracle's codes
+    for every input without NaN; NaN elements give NaN codes on both sides).
+    The fp32 quotients themselves may differ in the last bit; those counts
+    are reported, not asserted."""
     counts = torch.zeros(4, dtype=torch.int64, device="cuda")
     first = torch.zeros(1, dtype=torch.int32, device="cuda")
     st = ep.ep_selftest_fp8_quotient(counts.data_ptr(), first.data_ptr(),

@@ -4,10 +4,11 @@ the same seeded inputs.
 Bars: layout, slot map, identity metadata, bf16 dispatch rows, FP8 payloads
 and scales are bit-exact; combine within 1 bf16 ulp, |d| <= 2^-7 |ref| + 1e-6
 (expected bit-exact: both sides fold in fp32 with fmaf in ascending k and
-cast once).  Small and medium cases are compared element by element; at the
-workloads' full sizes, whole outputs are compared where the oracle finishes
-in seconds, otherwise sampled tokens are recomputed by the oracle one by one
-and every row is checked against properties that hold at any size.
+cast once).  Every case is compared element by element, the workloads' full
+sizes included: the oracle defines each dispatched row token by token, so its
+rows are computed once per token and every copy the GPU wrote is compared
+with them.  NaN results compare by NaN-ness (IEEE leaves the sign of an
+invalid operation's NaN open, so an E4M3 NaN code may be 0x7F or 0xFF).
 """
 
 import numpy as np
@@ -245,6 +246,53 @@ def test_bounded_wait_times_out_cleanly(ep):
     assert float(torch.ones(3, device="cuda").sum()) == 3.0
 
 
+def _stream_ptr():
+    return torch.cuda.current_stream().cuda_stream
+
+
+@pytest.mark.parametrize("stall_tile,timeout_ns", [(1, 1000), (77, 1_000_000), (151, 1000)])
+def test_layout_own_wait_times_out_and_is_reported(ep, stall_tile, timeout_ns):
+    """The two-launch layout's bounded wait, run out in one CTA other than 0:
+    with a 1 us limit that CTA records the timeout before CTA 0 publishes the
+    routing errors, and the publish keeps it (OR, not a store); with 1 ms it
+    records after.  Either way the status is EP_ERR_TIMEOUT, the context stays
+    usable, and the next good layout reports EP_OK and is exact."""
+    wl = workloads.WORKLOADS["prefill"]          # 128 token tiles, 152 CTAs
+    inp = inputs(wl)
+    cfg = cfg_of(ep, wl)
+    idx = dev(inp["topk_idx"])
+    L = ep.Layout(cfg)
+    st = ep.ep_selftest_layout_timeout(cfg.c(), wl.num_tokens, idx.data_ptr(), L.c,
+                                       stall_tile, timeout_ns, _stream_ptr())
+    assert st == ep.EP_ERR_TIMEOUT, ep.ep_status_str(st)
+    assert ep.ep_check_error(L.c, _stream_ptr()) == ep.EP_ERR_TIMEOUT
+    assert float(torch.ones(3, device="cuda").sum()) == 3.0
+    ep.get_layout(cfg, idx, layout=L, sync=True)
+    assert ep.check_error(L) == ep.EP_OK
+    assert_layout_equal(L, oracle_layout(wl, inp["topk_idx"], cfg.capacity), wl.num_tokens)
+
+
+def test_layout_timeout_in_cta0_replaces_earlier_status(ep):
+    """CTA 0 (the one that publishes) runs out of time after a call that left
+    a routing error in the word: the word was cleared at the start of the
+    call, so the status is the timeout alone, never the earlier error."""
+    wl = workloads.WORKLOADS["skew"]
+    inp = inputs(wl)
+    cfg = cfg_of(ep, wl)
+    bad = inp["topk_idx"].copy()
+    bad[5, 1] = wl.num_experts                   # out of range
+    L = ep.Layout(cfg)
+    ep.get_layout(cfg, dev(bad), layout=L, sync=False)
+    assert ep.check_error(L) == ep.EP_ERR_EXPERT_RANGE
+    idx = dev(inp["topk_idx"])
+    st = ep.ep_selftest_layout_timeout(cfg.c(), wl.num_tokens, idx.data_ptr(), L.c, 0,
+                                       1000, _stream_ptr())
+    assert st == ep.EP_ERR_TIMEOUT, ep.ep_status_str(st)
+    ep.get_layout(cfg, idx, layout=L, sync=True)
+    assert ep.check_error(L) == ep.EP_OK
+    assert_layout_equal(L, oracle_layout(wl, inp["topk_idx"], cfg.capacity), wl.num_tokens)
+
+
 # --------------------------------------------------------------------------
 # dispatch
 # --------------------------------------------------------------------------
@@ -279,83 +327,113 @@ def test_dispatch_bf16_bit_exact(ep, name, zp):
     assert np.array_equal(got_w[rows], ref_w[:used][rows])
 
 
-@pytest.mark.parametrize("name", ["sweep16k", "sweep4k"])
-def test_dispatch_bf16_full_size_rows(ep, name):
-    """Every row in use is the bit copy of its source token (a property the
-    oracle's definition fixes at any size), plus the oracle's own rows for a
-    sample of tokens."""
-    wl = workloads.WORKLOADS[name]
-    inp, cfg, L, ora, recv_x, _, recv_w = _dispatch_case(ep, wl, False)
-    used = int(ora["expert_start"][-1])
-    src = ora["src_info"][:used]
-    rows = np.nonzero(src[:, 0] >= 0)[0]
-    got = host_u16(recv_x[:used])
-    assert np.array_equal(got[rows], inp["x"][src[rows, 0]])
-    assert np.array_equal(recv_w[:used].cpu().numpy()[rows],
-                          inp["topk_weights"][src[rows, 0], src[rows, 1]])
-    rng = np.random.default_rng(9)
-    toks = np.unique(np.concatenate([[0, wl.num_tokens - 1], rng.choice(wl.num_tokens, 64)]))
-    sub = {**ora, "slot_of": np.arange(toks.size, dtype=np.int32).reshape(-1, 1),
-           "cap": toks.size}
-    sub["expert_start"] = np.array([0, toks.size], np.int32)
-    sub["expert_end"] = np.array([toks.size], np.int32)
-    sub["expert_count"] = np.array([toks.size], np.int32)
-    ref, _ = oracle.dispatch_bf16(inp["x"][toks], None, sub)
-    for i, t in enumerate(toks):
-        for s in ora["slot_of"][t]:
-            if s >= 0:
-                assert np.array_equal(got[s], ref[i])
+def _identity_slots(n):
+    """A layout of n tokens with one row each (row i = token i)."""
+    return {"slot_of": np.arange(n, dtype=np.int32).reshape(-1, 1), "cap": n,
+            "expert_start": np.array([0, n], np.int32), "expert_end": np.array([n], np.int32),
+            "expert_count": np.array([n], np.int32)}
 
 
 def _fp8_oracle_rows(x_rows):
     """Oracle quantisation of each given bf16 row (one slot per row)."""
-    n = x_rows.shape[0]
-    sub = {"slot_of": np.arange(n, dtype=np.int32).reshape(-1, 1), "cap": n,
-           "expert_start": np.array([0, n], np.int32), "expert_end": np.array([n], np.int32),
-           "expert_count": np.array([n], np.int32)}
-    q, s, _ = oracle.dispatch_fp8(x_rows, None, sub)
+    q, s, _ = oracle.dispatch_fp8(x_rows, None, _identity_slots(x_rows.shape[0]))
     return q, s
+
+
+def _bf16_oracle_rows(x_rows):
+    """Oracle dispatch of each given bf16 row (one slot per row)."""
+    r, _ = oracle.dispatch_bf16(x_rows, None, _identity_slots(x_rows.shape[0]))
+    return r
+
+
+def _canon_e4m3(q):
+    """E4M3 codes with both NaN codes (S.1111.111) mapped to 0x7F."""
+    return torch.where((q & 0x7F) == 0x7F, torch.full_like(q, 0x7F), q)
+
+
+def assert_rows_equal_oracle(inp, ora, fp8, recv, recv_s=None, recv_w=None,
+                             zero_padding=False, chunk=4096):
+    """Every row in use against the oracle's rows, element by element.
+
+    The oracle's dispatch defines the row of each unmasked (t, k) from x[t]
+    alone, so its rows are computed once per token and compared with every
+    copy the GPU wrote (rows slot_of[t, k] for all k).  Weights ride along
+    per (t, k); alignment gap rows are all-zero bits when zero_padding."""
+    x, w = inp["x"], inp["topk_weights"]
+    T = x.shape[0]
+    if fp8:
+        ref_q, ref_s = _fp8_oracle_rows(x)
+        ref = torch.from_numpy(ref_q).cuda()
+        ref_sc = torch.from_numpy(ref_s.view(np.int32)).cuda()
+        got = recv
+        got_sc = recv_s.view(torch.int32)
+    else:
+        ref = torch.from_numpy(_bf16_oracle_rows(x).view(np.int16)).cuda()
+        got = recv.view(torch.int16)
+    slot = torch.from_numpy(ora["slot_of"]).cuda().long()
+    m = slot >= 0
+    tok = torch.arange(T, device="cuda").unsqueeze(1).expand_as(slot)[m]
+    kk = torch.arange(slot.shape[1], device="cuda").unsqueeze(0).expand_as(slot)[m]
+    sl = slot[m]
+    for c in range(0, sl.numel(), chunk):
+        s_, t_ = sl[c:c + chunk], tok[c:c + chunk]
+        if fp8:
+            assert torch.equal(_canon_e4m3(got[s_]), _canon_e4m3(ref[t_]))
+            assert torch.equal(got_sc[s_], ref_sc[t_])
+        else:
+            assert torch.equal(got[s_], ref[t_])
+    if recv_w is not None:
+        w_d = torch.from_numpy(w).cuda()
+        assert torch.equal(recv_w[sl].view(torch.int32), w_d[tok, kk].view(torch.int32))
+    if zero_padding:
+        used = int(ora["expert_start"][-1])
+        pad = torch.from_numpy(np.nonzero(ora["src_info"][:used, 0] < 0)[0]).cuda().long()
+        if pad.numel():
+            assert int((got[pad] != 0).sum()) == 0
+            if fp8:
+                assert int((got_sc[pad] != 0).sum()) == 0
+            if recv_w is not None:
+                assert int((recv_w[pad] != 0).sum()) == 0
+
+
+@pytest.mark.parametrize("name", ["sweep16k", "sweep4k", "prefill"])
+def test_dispatch_bf16_full_size(ep, name):
+    """Every row in use at full size against the oracle's rows."""
+    wl = workloads.WORKLOADS[name]
+    inp, cfg, L, ora, recv_x, _, recv_w = _dispatch_case(ep, wl, False)
+    assert_layout_equal(L, ora, wl.num_tokens)
+    assert_rows_equal_oracle(inp, ora, False, recv_x, recv_w=recv_w)
 
 
 @pytest.mark.parametrize("name,zp", [("decode", False), ("ragged_fp8", True),
                                      ("ragged_fp8", False), ("wide_experts", True),
                                      ("skew_small", False), ("skew", False),
-                                     ("sweep1k_fp8", False), ("sweep16k_fp8", False)])
+                                     ("sweep1k_fp8", False), ("sweep16k_fp8", False),
+                                     ("decode", True)])
 def test_dispatch_fp8_bit_exact(ep, name, zp):
     wl = workloads.WORKLOADS.get(name) or MEDIUM[name]
     inp, cfg, L, ora, recv_q, recv_s, recv_w = _dispatch_case(ep, wl, zp)
-    used = int(ora["expert_start"][-1])
-    got_q = recv_q[:used].cpu().numpy()
-    got_s = recv_s[:used].cpu().numpy()
-    got_w = recv_w[:used].cpu().numpy()
+    assert_rows_equal_oracle(inp, ora, True, recv_q, recv_s, recv_w, zero_padding=zp)
     if wl.num_tokens * wl.num_topk <= 20000:
+        # and the oracle's own dispatch call, row for row
+        used = int(ora["expert_start"][-1])
         ref_q, ref_s, ref_w = oracle.dispatch_fp8(inp["x"], inp["topk_weights"], ora,
                                                   zero_padding=zp)
         rows = ora["src_info"][:used, 0] >= 0
         if zp:
             rows[:] = True
-        assert np.array_equal(got_q[rows], ref_q[:used][rows])
-        assert np.array_equal(got_s[rows].view(np.uint32), ref_s[:used][rows].view(np.uint32))
-        assert np.array_equal(got_w[rows], ref_w[:used][rows])
-    else:
-        # sampled tokens, every copy of each
-        rng = np.random.default_rng(10)
-        toks = np.unique(np.concatenate([[0, wl.num_tokens - 1],
-                                         rng.choice(wl.num_tokens, 256)]))
-        ref_q, ref_s = _fp8_oracle_rows(inp["x"][toks])
-        for i, t in enumerate(toks):
-            for k, s in enumerate(ora["slot_of"][t]):
-                if s >= 0:
-                    assert np.array_equal(got_q[s], ref_q[i])
-                    assert np.array_equal(got_s[s].view(np.uint32), ref_s[i].view(np.uint32))
-                    assert got_w[s] == inp["topk_weights"][t, k]
+        assert np.array_equal(recv_q[:used].cpu().numpy()[rows], ref_q[:used][rows])
+        assert np.array_equal(recv_s[:used].cpu().numpy()[rows].view(np.uint32),
+                              ref_s[:used][rows].view(np.uint32))
+        assert np.array_equal(recv_w[:used].cpu().numpy()[rows], ref_w[:used][rows])
 
 
-def test_dispatch_fp8_special_rows(ep):
-    """Zero blocks, saturation-size values, tiny values, signed zeros, and
-    rows whose block scales lie on both sides of 2^-100 (below it the
-    dispatch divides; above it, reciprocal product plus FMA correction)."""
-    T, H = 16, 512
+def _special_fp8_rows():
+    """Zero blocks, saturation-size values, tiny values, signed zeros, rows
+    whose block scales lie on both sides of 2^-100 (below it the dispatch
+    divides; above it, reciprocal product plus FMA correction), and blocks
+    holding +-inf or NaN next to finite values."""
+    T, H = 22, 512
     rng = np.random.default_rng(12)
     xf = rng.standard_normal((T, H)).astype(np.float32)
     xf[0] = 0.0                                 # all-zero row: scale 0, q 0
@@ -367,17 +445,55 @@ def test_dispatch_fp8_special_rows(ep):
     xf[6, 5] = 3.0e38                           # one block dominated by one value
     for r, e in zip(range(8, 16), [-90, -95, -99, -100, -101, 60, 100, 120]):
         xf[r] *= np.float32(2.0 ** e)
-    x = workloads.to_bf16_bits(xf)
+    # non-finite values: the block scale is +inf, finite neighbours encode
+    # as +-0, the infinities themselves as NaN codes (inf / inf)
+    xf[16, 3] = np.inf                          # +inf in block 0
+    xf[16, 130] = -np.inf                       # -inf in block 1
+    xf[16, 300] = np.inf                        # both signs in block 2
+    xf[16, 301] = -np.inf
+    xf[17, :] = np.inf                          # a whole row of +inf
+    xf[18, ::3] = -np.inf                       # -inf every third element
+    xf[19, 7] = np.nan                          # NaN next to finite values:
+    xf[19, 200] = np.nan                        #   ignored by amax
+    xf[20, 9] = np.nan                          # NaN and inf in one block
+    xf[20, 10] = np.inf
+    xf[21, :128] = np.nan                       # an all-NaN block: scale 0
+    return workloads.to_bf16_bits(xf)
+
+
+def test_dispatch_fp8_special_rows(ep):
+    x = _special_fp8_rows()
+    T, H = x.shape
     idx = np.array([[t % 4, 4 + t % 4] for t in range(T)], np.int64)
+    w = np.full((T, 2), 0.5, np.float32)
     wl = workloads.Workload("fp8s", T, H, 8, 2, 2, True, expert_alignment=4)
     cfg = cfg_of(ep, wl, zero_padding=True)
-    L = run_layout(ep, cfg, idx)
-    recv_q, recv_s, _ = ep.dispatch(cfg, L, dev_bf16(x))
     ora = oracle_layout(wl, idx, cfg.capacity)
-    ref_q, ref_s, _ = oracle.dispatch_fp8(x, None, ora, zero_padding=True)
+    inp = {"x": x, "topk_weights": w}
+    ref_q, ref_s, ref_w = oracle.dispatch_fp8(x, w, ora, zero_padding=True)
     used = int(ora["expert_start"][-1])
-    assert np.array_equal(recv_q[:used].cpu().numpy(), ref_q[:used])
-    assert np.array_equal(recv_s[:used].cpu().numpy().view(np.uint32), ref_s[:used].view(np.uint32))
+    # the separate calls, and layout and dispatch in one call (one kernel here)
+    L = run_layout(ep, cfg, idx)
+    got = [ep.dispatch(cfg, L, dev_bf16(x), dev(w))]
+    L2, rq2, rs2, rw2 = ep.layout_and_dispatch(cfg, dev(idx), dev_bf16(x), dev(w))
+    torch.cuda.synchronize()
+    assert ep.check_error(L2) == ep.EP_OK
+    assert_layout_equal(L2, ora, T)
+    got.append((rq2, rs2, rw2))
+    for rq, rs, rw in got:
+        assert_rows_equal_oracle(inp, ora, True, rq, rs, rw, zero_padding=True)
+        q = rq[:used].cpu().numpy()
+        nan_ref = (ref_q[:used] & 0x7F) == 0x7F
+        assert np.array_equal((q & 0x7F) == 0x7F, nan_ref)
+        assert np.array_equal(q[~nan_ref], ref_q[:used][~nan_ref])
+        assert np.array_equal(rs[:used].cpu().numpy().view(np.uint32),
+                              ref_s[:used].view(np.uint32))
+        assert np.array_equal(rw[:used].cpu().numpy(), ref_w[:used])
+    # the readings themselves: an infinite block has scale +inf and its
+    # finite elements encode as +-0
+    r16 = ora["slot_of"][16, 0]
+    assert np.all(np.isinf(ref_s[r16, :3])) and ref_s[r16, 3] != np.inf
+    assert set(np.unique(ref_q[r16, :128][np.arange(128) != 3])) <= {0x00, 0x80}
 
 
 def test_dispatch_reuses_layout_and_stream(ep):
@@ -424,8 +540,9 @@ def test_combine_full_compare(ep, name, weighted):
     assert np.array_equal(got, ref)   # expected bit-exact (same fold, same cast)
 
 
-@pytest.mark.parametrize("name", ["prefill", "skew", "sweep16k"])
-def test_combine_full_size_sampled(ep, name):
+@pytest.mark.parametrize("name", ["prefill", "skew", "sweep16k", "sweep1k"])
+def test_combine_full_size(ep, name):
+    """Every token at full size against the oracle's fold."""
     wl = workloads.WORKLOADS[name]
     inp = inputs(wl)
     cfg = cfg_of(ep, wl)
@@ -434,16 +551,39 @@ def test_combine_full_size_sampled(ep, name):
     y = ep.combine(cfg, L, Y, dev(inp["topk_weights"]))
     torch.cuda.synchronize()
     ora = oracle_layout(wl, inp["topk_idx"], cfg.capacity)
-    rng = np.random.default_rng(13)
-    toks = np.unique(np.concatenate([[0, wl.num_tokens - 1], rng.choice(wl.num_tokens, 512)]))
-    rows = ora["slot_of"][toks]
-    need = np.unique(rows[rows >= 0])
-    Yh = np.zeros((cfg.capacity, cfg.hidden), np.uint16)
-    Yh[need] = host_u16(Y[torch.from_numpy(need).long().cuda()])
-    ref = oracle.combine_tokens(Yh, inp["topk_weights"], ora["slot_of"], toks)
-    got = host_u16(y)[toks]
+    used = int(ora["expert_start"][-1])
+    ref = oracle.combine(host_u16(Y[:used]), inp["topk_weights"], ora["slot_of"])
+    got = host_u16(y)
     assert_combine_close(got, ref)
     assert np.array_equal(got, ref)
+
+
+def test_combine_non_finite_rows(ep):
+    """Expert rows holding +-inf and NaN: the fold propagates them as the
+    oracle's does (inf + -inf and 0 * inf give NaN); NaN results compare by
+    NaN-ness (the sign of an invalid operation's NaN is not fixed by IEEE),
+    everything else bit-exact."""
+    wl = MEDIUM["ragged_bf16"]
+    inp = inputs(wl)
+    cfg = cfg_of(ep, wl)
+    L = run_layout(ep, cfg, inp["topk_idx"])
+    Yh = host_u16(_expert_out(cfg, 3))
+    rng = np.random.default_rng(14)
+    cells = rng.integers(0, Yh.size, 4000)
+    Yh.reshape(-1)[cells[:1500]] = 0x7F80          # +inf
+    Yh.reshape(-1)[cells[1500:3000]] = 0xFF80      # -inf
+    Yh.reshape(-1)[cells[3000:]] = 0x7FC0          # NaN
+    w = inp["topk_weights"].copy()
+    w[::7, 0] = 0.0                                # 0 * inf
+    y = ep.combine(cfg, L, dev_bf16(Yh), dev(w))
+    torch.cuda.synchronize()
+    ora = oracle_layout(wl, inp["topk_idx"], cfg.capacity)
+    ref = oracle.combine(Yh, w, ora["slot_of"])
+    got = host_u16(y)
+    nan = lambda u: ((u & 0x7F80) == 0x7F80) & ((u & 0x7F) != 0)
+    assert nan(ref).any() and ((ref & 0x7FFF) == 0x7F80).any()
+    assert np.array_equal(nan(got), nan(ref))
+    assert np.array_equal(got[~nan(ref)], ref[~nan(ref)])
 
 
 @pytest.mark.parametrize("name", ["prefill", "sweep16k", "decode"])
@@ -544,6 +684,8 @@ def test_layout_and_dispatch_equals_separate_calls(ep, name, zp):
     assert_layout_equal(L2, ora, wl.num_tokens)
     used = int(ora["expert_start"][-1])
     rows = np.arange(used) if zp else np.nonzero(ora["src_info"][:used, 0] >= 0)[0]
+    # against the oracle directly, then against the separate calls
+    assert_rows_equal_oracle(inp, ora, cfg.use_fp8_dispatch, rx2, rs2, rw2, zero_padding=zp)
     r = torch.from_numpy(rows).long().cuda()
     assert torch.equal(rx2[r].view(torch.uint8), rx1[r].view(torch.uint8))
     if cfg.use_fp8_dispatch:

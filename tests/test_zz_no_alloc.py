@@ -79,3 +79,29 @@ def test_noalloc_rejects_configs_beyond_its_scratch(ep):
     idx = torch.zeros((1024, 8), dtype=torch.int64, device="cuda")
     st = ep.ep_get_layout_noalloc(cfg.c(), 1024, idx.data_ptr(), L.c, None, _stream())
     assert st == ep.EP_ERR_CAPACITY
+
+
+def test_noalloc_small_layout_needs_no_scratch(ep):
+    """A layout of at most 4096 (t, k) pairs takes one launch and uses no
+    scratch, so the allocation-free entry point accepts it even where the
+    two-launch scratch would exceed the array (2048 experts, 2048 ranks)."""
+    cfg = ep.Config(512, 128, 8, 2048, 2048, 4)
+    assert ep.ep_layout_workspace_bytes(cfg.c()) > (1 << 20)
+    rng = np.random.default_rng(21)
+    idx_np = workloads.random_routes(rng, 512, 2048, 8)
+    idx = torch.from_numpy(idx_np).cuda()
+    ref_L, na_L = ep.Layout(cfg), ep.Layout(cfg)
+    na_L.c.workspace = None
+    for _ in range(2):
+        assert ep.ep_get_layout(cfg.c(), 512, idx.data_ptr(), ref_L.c, None, _stream()) == ep.EP_OK
+        st = ep.ep_get_layout_noalloc(cfg.c(), 512, idx.data_ptr(), na_L.c, None, _stream())
+        assert st == ep.EP_OK, ep.ep_status_str(st)
+        torch.cuda.synchronize()
+        a, b = _host(na_L), _host(ref_L)
+        used = int(b["expert_start"][-1])
+        for f in FIELDS:
+            if f == "src_info":
+                assert np.array_equal(a[f][:used], b[f][:used]), f
+            else:
+                assert np.array_equal(a[f], b[f]), f
+        assert ep.ep_check_error(na_L.c, _stream()) == ep.EP_OK
