@@ -281,10 +281,20 @@ def job_throughput(tokens_per_rank: int, ms_local: float, world: int, device=Non
 # CPU oracle timing (baseline / reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_step_fn(wl, inp):
+def host_cores() -> int:
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_step_fn(wl, inp, nthreads=1):
     """One oracle step over the given inputs: layout -> dispatch -> combine
     (identity experts: combine reads the dispatched rows).  Output buffers are
-    allocated once, outside the timing."""
+    allocated once, outside the timing.  nthreads > 1: dispatch and combine
+    run on token slices in that many threads (the oracle's own functions, same
+    results); the layout stays sequential."""
     import numpy as np
 
     import oracle
@@ -303,23 +313,18 @@ def oracle_step_fn(wl, inp):
                             wl.expert_alignment, cap=cap)
         if wl.use_fp8_dispatch:
             # FP8 payload for the wire, bf16 rows for the experts' identity output
-            L = oracle.lib()
-            L.oracle_dispatch_fp8(T, H, K, wl.num_experts, oracle._ptr(inp["x"]),
-                                  oracle._ptr(inp["topk_weights"]),
-                                  oracle._ptr(lay["slot_of"]),
-                                  oracle._ptr(lay["expert_start"]),
-                                  oracle._ptr(lay["expert_end"]), 0,
-                                  oracle._ptr(recv_q), oracle._ptr(recv_s),
-                                  oracle._ptr(recv_w))
-        oracle.dispatch_bf16(inp["x"], inp["topk_weights"], lay, out=(recv_x, recv_w))
-        oracle.combine(recv_x, inp["topk_weights"], lay["slot_of"], out=y)
+            oracle.dispatch_fp8(inp["x"], inp["topk_weights"], lay,
+                                out=(recv_q, recv_s, recv_w), nthreads=nthreads)
+        oracle.dispatch_bf16(inp["x"], inp["topk_weights"], lay, out=(recv_x, recv_w),
+                             nthreads=nthreads)
+        oracle.combine(recv_x, inp["topk_weights"], lay["slot_of"], out=y, nthreads=nthreads)
         return y
 
     return step
 
 
-def time_oracle(wl, inp, budget_s, min_steps=1, max_steps=1000):
-    step = oracle_step_fn(wl, inp)
+def time_oracle(wl, inp, budget_s, min_steps=1, max_steps=1000, nthreads=1):
+    step = oracle_step_fn(wl, inp, nthreads)
     times = []
     t_start = time.perf_counter()
     while len(times) < max_steps:
@@ -339,15 +344,22 @@ def subsample(inp, wl, n_tokens):
 
 
 def cpu_baseline(wl, inp, budget_s):
-    """The oracle as it stands, single-threaded, on a bounded sample."""
+    """The oracle as it stands on a bounded sample: on all the host's cores
+    (dispatch and combine on token slices, one thread a core; layout
+    sequential), and single-threaded beside it."""
     n = wl.num_tokens
-    times = time_oracle(wl, inp, budget_s)
-    total = sum(times)
-    return {"value": n * len(times) / total, "unit": "tokens/s", "cores": 1,
+    cores = host_cores()
+    mt = time_oracle(wl, inp, budget_s / 2, nthreads=cores)
+    st = time_oracle(wl, inp, budget_s / 2)
+    what = f"(T={n}; layout+dispatch+combine, identity experts)"
+    return {"value": n * len(mt) / sum(mt), "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"{len(times)} full step(s) of the same workload "
-                      f"(T={n}; layout+dispatch+combine, identity experts), "
-                      f"{total:.1f} s of CPU time on 1 thread"}
+            "sample": f"{len(mt)} full step(s) of the same workload {what}, "
+                      f"{sum(mt):.1f} s wall on {cores} threads (dispatch and combine "
+                      "split over tokens; layout sequential)",
+            "single_thread": {"value": n * len(st) / sum(st), "unit": "tokens/s", "cores": 1,
+                              "sample": f"{len(st)} full step(s) {what}, {sum(st):.1f} s "
+                                        "on 1 thread"}}
 
 
 def run_reference(args):
@@ -361,15 +373,16 @@ def run_reference(args):
         return 0
     wl = workloads.WORKLOADS[args.workload]
     inp = workloads.make_inputs(wl, seed=0)
+    cores = host_cores()
     # size each step's sample so that warm-up + timed steps take ~60 s at most
-    cal_n = min(wl.num_tokens, 64)
+    cal_n = min(wl.num_tokens, 64 * cores)
     s_inp, s_wl = subsample(inp, wl, cal_n)
-    t = time_oracle(s_wl, s_inp, 0.0, min_steps=2, max_steps=2)
+    t = time_oracle(s_wl, s_inp, 0.0, min_steps=2, max_steps=2, nthreads=cores)
     per_token = max(min(t) / cal_n, 1e-7)
     budget = 60.0 / max(1, args.steps + args.warmup)
     n = int(max(16, min(wl.num_tokens, budget / per_token)))
     s_inp, s_wl = subsample(inp, wl, n)
-    step = oracle_step_fn(s_wl, s_inp)
+    step = oracle_step_fn(s_wl, s_inp, nthreads=cores)
     for _ in range(args.warmup):
         step()
     times = []
@@ -383,12 +396,14 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16",
+        "vs_baseline": None, "dtype": path_dtype(wl),
         "data": "synthetic (seeded router simulation)",
         "config": workload_config(wl, extra={"sample_tokens_per_step": n}),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"first {n} of {wl.num_tokens} tokens per step "
-                                   "(same E/K/R/H), layout+dispatch+combine, identity experts"},
+                                   "(same E/K/R/H), layout+dispatch+combine, identity experts; "
+                                   f"dispatch and combine on {cores} threads (token slices), "
+                                   "layout sequential"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -408,6 +423,12 @@ def e2e_transfer(requested: str, device_entry_points_only: bool) -> str:
     if device_entry_points_only:
         return "copies"
     return "direct" if requested == "auto" else requested
+
+
+def path_dtype(wl) -> str:
+    """The arithmetic of the path: E4M3 rows (fp32 quantisation) or bf16 bit
+    copies on dispatch; the combine folds bf16 rows in fp32 either way."""
+    return "fp8_e4m3" if wl.use_fp8_dispatch else "bf16"
 
 
 def workload_config(wl, extra=None):
@@ -678,6 +699,22 @@ def run_ours(args):
         e[ns].record(stream)
     torch.cuda.synchronize()
     barrier(world)
+    # Steady state: the same steps back to back with no flush between them,
+    # one event pair around all K, so that each step's write-back of the
+    # lines it left dirty in L2 lands inside the timing (of the next step).
+    for _ in range(args.warmup):
+        for fn in step_runners:
+            fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    ss = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ss[0].record(stream)
+    for i in range(args.steps):
+        for fn in step_runners:
+            fn()
+    ss[1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
     t1 = time.perf_counter()
     sampler.stop()
     clocks = sampler.summary(t0, t1)
@@ -725,6 +762,16 @@ def run_ours(args):
                 "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                 else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": b[dom]}
+    ss_value, ss_ms = job_throughput(T, ss[0].elapsed_time(ss[1]) / args.steps, world, device)
+    touched = sum(b[n] for n in streaming)
+    steady = {"value": ss_value, "unit": "tokens/s", "ms_per_step": ss_ms,
+              "timing": (f"{args.steps} steps back to back, no L2 flush between them, one "
+                         "event pair around all of them (each step's L2 write-back lands "
+                         "inside the timing)"),
+              "fits_in_l2": touched < 126 * 2**20}
+    if steady["fits_in_l2"]:
+        steady["note"] = ("the bytes one step touches fit in L2: later steps find their "
+                          "inputs cached, so this is not a DRAM-bound figure")
     stream_ms = sum(avg.values())
     breakdown = {"layout_us": (1e3 * statistics.mean(stage_ms["layout"]) if "layout" in stage_ms
                                else None)}
@@ -740,6 +787,20 @@ def run_ours(args):
     })
     if ranks_pass:
         breakdown["rank_rows"] = n_rank_rows
+    if args.zero_padding and not (backward or ranks_pass):
+        # the dispatch stage also clears the alignment gap rows: their bytes,
+        # counted apart from the algorithmic bytes above
+        used = int(L.expert_start[-1])
+        rowbytes = (H + 4 * (H // 128)) if wl.use_fp8_dispatch else 2 * H
+        pad_rows = used - n_rows
+        pad_bytes = pad_rows * (rowbytes + 4)
+        dname = "layout_dispatch" if args.fused else "dispatch"
+        breakdown.update({
+            "zero_padding_rows": pad_rows, "zero_padding_bytes": pad_bytes,
+            f"{dname}_gbs_note": ("excludes the zero-padding bytes; the stage time "
+                                  "includes clearing them"),
+            f"{dname}_gbs_incl_padding": (b[dname] + pad_bytes) / (avg[dname] * 1e-3) / 1e9,
+        })
 
     # ---- end to end through the API, host buffers ----------------------------
     e2e = None
@@ -826,7 +887,8 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic (seeded router simulation, PCG64; no dataset)",
+            "dtype": path_dtype(wl),
+            "data": "synthetic (seeded router simulation, PCG64; no dataset)",
             "config": workload_config(wl, extra={
                 "l2": "flushed before every step (256 MiB write, then 256 MiB read), outside the step events",
                 "timing": ("step: events around each whole step; stage times and the roofline "
@@ -845,6 +907,7 @@ def run_ours(args):
                 "layout_and_dispatch": ("one call, one kernel" if args.fused and fused_small
                                         else "one call" if args.fused else "separate calls")}),
             "roofline": roofline,
+            "steady_state": steady,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,

@@ -21,20 +21,24 @@ import numpy as np
 
 _DIR = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_DIR, "ep_oracle.c")
+_SRC_MT = os.path.join(_DIR, "ep_oracle_mt.c")
 _LIB = os.path.join(_DIR, "libep_oracle.so")
 
 OK, ERR_INVALID_ARG, ERR_EXPERT_RANGE, ERR_DUP_EXPERT, ERR_CAPACITY = range(5)
 
 
 def build_oracle(force: bool = False) -> str:
-    """Compile ``ep_oracle.c`` into ``libep_oracle.so`` next to it."""
+    """Compile ``ep_oracle.c`` (and its multi-threaded driver
+    ``ep_oracle_mt.c``) into ``libep_oracle.so`` next to them."""
+    srcs = [_SRC, _SRC_MT, os.path.join(_DIR, "ep_oracle.h")]
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(
-        os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_DIR, "ep_oracle.h"))
+        os.path.getmtime(f) for f in srcs
     ):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(
             ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-             "-fPIC", "-shared", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+             "-fPIC", "-shared", "-pthread", "-Wall", "-Wextra", "-o", tmp, _SRC, _SRC_MT,
+             "-lm"]
         )
         os.replace(tmp, _LIB)
     return _LIB
@@ -81,6 +85,14 @@ def _declare(L):
                                       ctypes.c_int, _p, _p, _p]
     L.oracle_combine.restype = None
     L.oracle_combine.argtypes = [_i32, _i32, _i32, _p, _p, _p, _p]
+    L.oracle_dispatch_bf16_mt.restype = ctypes.c_int
+    L.oracle_dispatch_bf16_mt.argtypes = [_i32, _i32, _i32, _i32, _p, _p, _p, _p, _p,
+                                          ctypes.c_int, _p, _p, _i32]
+    L.oracle_dispatch_fp8_mt.restype = ctypes.c_int
+    L.oracle_dispatch_fp8_mt.argtypes = [_i32, _i32, _i32, _i32, _p, _p, _p, _p, _p,
+                                         ctypes.c_int, _p, _p, _p, _i32]
+    L.oracle_combine_mt.restype = ctypes.c_int
+    L.oracle_combine_mt.argtypes = [_i32, _i32, _i32, _p, _p, _p, _p, _i32]
     L.oracle_combine_epilogue.restype = None
     L.oracle_combine_epilogue.argtypes = [_i32, _i32, _i32] + [_p] * 8
     L.oracle_dispatch_backward.restype = None
@@ -190,9 +202,11 @@ def layout(topk_idx: np.ndarray, num_experts: int, num_ranks: int,
 
 
 def dispatch_bf16(x, topk_weights, lay: dict, zero_padding=False, fill=0xFFFF,
-                  out=None):
+                  out=None, nthreads=1):
     """Expanded bf16 dispatch; rows the method does not write keep ``fill``
-    (or their previous contents when ``out=(recv_x, recv_w)`` is given)."""
+    (or their previous contents when ``out=(recv_x, recv_w)`` is given).
+    nthreads > 1 runs the same function on token slices in that many threads
+    (identical result)."""
     x = _c(x, np.uint16)
     T, H = x.shape
     slot_of = _c(lay["slot_of"], np.int32)
@@ -207,15 +221,21 @@ def dispatch_bf16(x, topk_weights, lay: dict, zero_padding=False, fill=0xFFFF,
     else:
         recv_x = np.full((cap, H), fill, np.uint16)
         recv_w = np.full(cap, np.nan, np.float32)
-    lib().oracle_dispatch_bf16(T, H, K, E, _ptr(x), _ptr(w), _ptr(slot_of),
-                               _ptr(_c(lay["expert_start"], np.int32)),
-                               _ptr(_c(lay["expert_end"], np.int32)),
-                               int(bool(zero_padding)), _ptr(recv_x), _ptr(recv_w))
+    args = (T, H, K, E, _ptr(x), _ptr(w), _ptr(slot_of),
+            _ptr(_c(lay["expert_start"], np.int32)), _ptr(_c(lay["expert_end"], np.int32)),
+            int(bool(zero_padding)), _ptr(recv_x), _ptr(recv_w))
+    if nthreads > 1:
+        lib().oracle_dispatch_bf16_mt(*args, int(nthreads))
+    else:
+        lib().oracle_dispatch_bf16(*args)
     return recv_x, recv_w
 
 
-def dispatch_fp8(x, topk_weights, lay: dict, zero_padding=False, fill=0xFF):
-    """Expanded dispatch with fused 1x128 E4M3 quantisation."""
+def dispatch_fp8(x, topk_weights, lay: dict, zero_padding=False, fill=0xFF, out=None,
+                 nthreads=1):
+    """Expanded dispatch with fused 1x128 E4M3 quantisation (``out=(recv_q,
+    recv_scale, recv_w)`` writes into given arrays; nthreads as in
+    dispatch_bf16)."""
     x = _c(x, np.uint16)
     T, H = x.shape
     slot_of = _c(lay["slot_of"], np.int32)
@@ -223,19 +243,28 @@ def dispatch_fp8(x, topk_weights, lay: dict, zero_padding=False, fill=0xFF):
     E = lay["expert_count"].shape[0]
     cap = lay["cap"]
     w = None if topk_weights is None else _c(topk_weights, np.float32)
-    recv_q = np.full((cap, H), fill, np.uint8)
-    recv_scale = np.full((cap, H // 128), np.nan, np.float32)
-    recv_w = np.full(cap, np.nan, np.float32)
-    lib().oracle_dispatch_fp8(T, H, K, E, _ptr(x), _ptr(w), _ptr(slot_of),
-                              _ptr(_c(lay["expert_start"], np.int32)),
-                              _ptr(_c(lay["expert_end"], np.int32)),
-                              int(bool(zero_padding)), _ptr(recv_q),
-                              _ptr(recv_scale), _ptr(recv_w))
+    if out is not None:
+        recv_q, recv_scale, recv_w = out
+        assert recv_q.shape == (cap, H) and recv_q.dtype == np.uint8
+        assert recv_scale.shape == (cap, H // 128) and recv_scale.dtype == np.float32
+        assert recv_w.shape == (cap,) and recv_w.dtype == np.float32
+    else:
+        recv_q = np.full((cap, H), fill, np.uint8)
+        recv_scale = np.full((cap, H // 128), np.nan, np.float32)
+        recv_w = np.full(cap, np.nan, np.float32)
+    args = (T, H, K, E, _ptr(x), _ptr(w), _ptr(slot_of),
+            _ptr(_c(lay["expert_start"], np.int32)), _ptr(_c(lay["expert_end"], np.int32)),
+            int(bool(zero_padding)), _ptr(recv_q), _ptr(recv_scale), _ptr(recv_w))
+    if nthreads > 1:
+        lib().oracle_dispatch_fp8_mt(*args, int(nthreads))
+    else:
+        lib().oracle_dispatch_fp8(*args)
     return recv_q, recv_scale, recv_w
 
 
-def combine(expert_out, topk_weights, slot_of, out=None) -> np.ndarray:
-    """Combine from the definition: returns y (uint16 bf16 bits [T, H])."""
+def combine(expert_out, topk_weights, slot_of, out=None, nthreads=1) -> np.ndarray:
+    """Combine from the definition: returns y (uint16 bf16 bits [T, H]);
+    nthreads as in dispatch_bf16."""
     Y = _c(expert_out, np.uint16)
     H = Y.shape[1]
     slot_of = _c(slot_of, np.int32)
@@ -246,7 +275,11 @@ def combine(expert_out, topk_weights, slot_of, out=None) -> np.ndarray:
         assert y.shape == (T, H) and y.dtype == np.uint16
     else:
         y = np.zeros((T, H), np.uint16)
-    lib().oracle_combine(T, H, K, _ptr(Y), _ptr(w), _ptr(slot_of), _ptr(y))
+    if nthreads > 1:
+        lib().oracle_combine_mt(T, H, K, _ptr(Y), _ptr(w), _ptr(slot_of), _ptr(y),
+                                int(nthreads))
+    else:
+        lib().oracle_combine(T, H, K, _ptr(Y), _ptr(w), _ptr(slot_of), _ptr(y))
     return y
 
 

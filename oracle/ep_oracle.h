@@ -191,6 +191,26 @@ void oracle_combine_ranks(int32_t T, int32_t H, int32_t R,
                           const int32_t *rank_slot_of, const uint16_t *rank_y,
                           uint16_t *y);
 
+/* ---- multi-threaded driver (ep_oracle_mt.c) ------------------------------
+ * The functions above, run by nthreads POSIX threads on contiguous token
+ * slices (no arithmetic of their own; results equal the single-threaded
+ * calls bit for bit).  Return 0, or -1 if a thread could not be started (the
+ * work is then finished on the calling thread). */
+int oracle_dispatch_bf16_mt(int32_t T, int32_t H, int32_t K, int32_t E,
+                            const uint16_t *x, const float *w,
+                            const int32_t *slot_of, const int32_t *expert_start,
+                            const int32_t *expert_end, int zero_padding,
+                            uint16_t *recv_x, float *recv_w, int32_t nthreads);
+int oracle_dispatch_fp8_mt(int32_t T, int32_t H, int32_t K, int32_t E,
+                           const uint16_t *x, const float *w,
+                           const int32_t *slot_of, const int32_t *expert_start,
+                           const int32_t *expert_end, int zero_padding,
+                           uint8_t *recv_q, float *recv_scale, float *recv_w,
+                           int32_t nthreads);
+int oracle_combine_mt(int32_t T, int32_t H, int32_t K, const uint16_t *Y,
+                      const float *w, const int32_t *slot_of, uint16_t *y,
+                      int32_t nthreads);
+
 #ifdef __cplusplus
 }
 #endif

@@ -37,3 +37,24 @@ def test_e2e_transfer_flag_choices_are_all_handled():
                                                                     "copies")
     finally:
         sys.argv = argv
+
+
+def test_path_dtype_follows_the_workload():
+    import workloads
+
+    assert bench.path_dtype(workloads.WORKLOADS["prefill"]) == "bf16"
+    for name in ("decode", "skew", "sweep16k_fp8"):
+        assert bench.path_dtype(workloads.WORKLOADS[name]) == "fp8_e4m3"
+
+
+def test_cpu_baseline_reports_all_cores_and_one():
+    """The CPU baseline times the oracle on every core it may use and on one
+    thread, on a bounded sample of the same workload."""
+    import workloads
+
+    wl = workloads.WORKLOADS["tiny"]
+    inp = workloads.make_inputs(wl, seed=0)
+    cb = bench.cpu_baseline(wl, inp, 0.2)
+    assert cb["cores"] == bench.host_cores() >= 1
+    assert cb["kind"] == "oracle" and cb["unit"] == "tokens/s" and cb["value"] > 0
+    assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
