@@ -14,6 +14,10 @@ namespace ep {
 // at least kMinTilePairs (t, k) pairs when the input allows.
 constexpr int kLayoutThreads = 256;
 constexpr int kLayoutWarps = kLayoutThreads / 32;
+// Threads of an assign-kernel CTA.  (1024, with the extra warps on the
+// column sums, scans and stores only, measured slower at 4K-16K tokens: the
+// larger CTAs start later.)
+constexpr int kAssignThreads = kLayoutThreads;
 constexpr int kLayoutMaxTiles = 152;
 constexpr int kMinTilePairs = 256;
 // The assign kernel loads the whole tile-count matrix with one bulk copy
@@ -26,9 +30,16 @@ constexpr int kScanChunkInts = 8192;
 // kSmallLayoutMaxExperts experts, take the one-launch layout.
 constexpr int kSmallLayoutPairs = 4096;
 constexpr int kSmallLayoutMaxExperts = 2048;
+// Threads of a one-launch layout CTA: a pair a thread at decode sizes, and
+// warps enough to hide the latency of its short dependent phases.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kSmallThreads / 32;
 bool layout_is_small(int64_t T, int K, int E);
 // Pairs a CTA of the one-launch layout may own when it also dispatches them.
 constexpr int kSmallOwnPairs = 64;
+// Shared memory up to which the one-launch layout also stages the x rows of
+// its own tokens when it dispatches them.
+constexpr int kSmallStageBudget = 200 * 1024;
 
 
 struct TileGeom {

@@ -211,6 +211,8 @@ __global__ void __launch_bounds__(kLayoutThreads)
 // ---------------------------------------------------------------------------
 
 // Block-wide exclusive scan of one int per thread (all threads must call).
+// s_warp[0..31] may be written again only after a __syncthreads() that
+// follows the call (every caller has one before its next use).
 __device__ __forceinline__ int block_exclusive_scan(int v, int32_t* s_warp,
                                                     int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -235,7 +237,6 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int32_t* s_warp,
   __syncthreads();
   const int warp_excl = warp > 0 ? s_warp[warp - 1] : 0;
   *total = s_warp[nw - 1];
-  __syncthreads();
   return warp_excl + x - v;
 }
 
@@ -252,8 +253,11 @@ __host__ __device__ inline AssignSmem assign_smem(int E, int R, int num_tiles) {
   const int Wc = Epad + Rpad;
   AssignSmem s;
   // column sums: 4 columns a thread; the threads left over take row groups
+  // (at most as many as keep the partial sums within 16 KB)
   const int col_groups = Wc / 4;
-  s.row_groups = col_groups < kLayoutThreads ? kLayoutThreads / col_groups : 1;
+  s.row_groups = col_groups < kAssignThreads ? kAssignThreads / col_groups : 1;
+  const int max_groups = 16384 / (8 * Wc);
+  if (s.row_groups > max_groups) s.row_groups = max_groups > 1 ? max_groups : 1;
   const int part_bytes = 2 * s.row_groups * Wc * 4;
   // bytes of everything but the count rows (barriers, histograms, scans,
   // partial sums)
@@ -285,7 +289,7 @@ __host__ __device__ inline AssignSmem assign_smem(int E, int R, int num_tiles) {
   return s;
 }
 
-__global__ void __launch_bounds__(kLayoutThreads)
+__global__ void __launch_bounds__(kAssignThreads)
     layout_assign_kernel(const int64_t* __restrict__ topk_idx, int T, int K,
                          int E, int R, int A, int tile_tokens, int num_tiles,
                          const int32_t* __restrict__ tile_counts,
@@ -319,6 +323,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
   int32_t* s_scr = reinterpret_cast<int32_t*>(smem + L.scratch);
   int32_t* s_part = reinterpret_cast<int32_t*>(smem + L.part);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
   const int tile = blockIdx.x;
   const bool has_tile = tile < num_tiles;
   int2* src_info2 = reinterpret_cast<int2*>(src_info);
@@ -363,7 +368,8 @@ __global__ void __launch_bounds__(kLayoutThreads)
   }
 
   // Pass 1 (overlaps the copies): per-warp histogram of this tile.  Warp w
-  // owns the contiguous pairs [pb, pe).
+  // < kLayoutWarps owns the contiguous pairs [pb, pe); the other warps own
+  // none (they join the column sums, scans and stores below).
   int t0 = 0, P = 0, pb = 0, pe = 0;
   int ignored = 0;
   if (has_tile) {
@@ -570,7 +576,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
       // one warp per rank: ballot over the tile's tokens, 32 at a time
       const int nt = min(tile_tokens, T - t0);
       const uint32_t lt = lanemask_lt();
-      for (int q = warp; q < R; q += kLayoutWarps) {
+      for (int q = warp; q < R; q += nwarps) {
         int run = s_rstart[q] + s_rbase[q];
         for (int c0 = 0; c0 < nt; c0 += 32) {
           const int t = t0 + c0 + lane;
@@ -587,7 +593,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
   }
 
   // Alignment padding rows carry no token (one warp per expert at a time).
-  for (int e = blockIdx.x * kLayoutWarps + warp; e < E; e += gridDim.x * kLayoutWarps) {
+  for (int e = blockIdx.x * nwarps + warp; e < E; e += gridDim.x * nwarps) {
     const int s0 = s_start[e] + s_total[e], s1 = s_start[e + 1];
     for (int s = s0 + lane; s < s1; s += 32) src_info2[s] = make_int2(-1, -1);
   }
@@ -604,14 +610,17 @@ __global__ void __launch_bounds__(kLayoutThreads)
 // kernel, rows for its own few tokens in (t, k) order, rank rows and
 // padding.  The rows are the same as the two-launch path's.
 struct SmallSmem {
-  int idx, hist, start, total, base, rcnt, rstart, scr, own, bytes;
+  int bar, idx, hist, start, total, base, rcnt, rstart, scr, own, rows, bytes;
 };
 
-__host__ __device__ inline SmallSmem small_smem(int E, int R) {
+// Shared-memory plan of the one-launch layout; with row_bytes > 0 it ends
+// with room for the rows of the CTA's own tokens (fused dispatch, staged).
+__host__ __device__ inline SmallSmem small_smem(int E, int R, int64_t row_bytes = 0) {
   const int Epad = padded_experts(E), Rpad = padded_ranks(R);
   SmallSmem s;
   int o = 0;
-  s.idx = o;    o += kSmallLayoutPairs * 4;        // the routes, checked, as int32
+  s.bar = o;    o += 16;                           // mbarrier of the staged rows
+  s.idx = o;    o += kSmallLayoutPairs * 4;        // the routes, checked, packed
   s.hist = o;   o += 3 * Epad * 4;                 // counts: earlier, own, later tokens
   s.start = o;  o += ((E + 1 + 3) & ~3) * 4;
   s.total = o;  o += Epad * 4;
@@ -620,9 +629,27 @@ __host__ __device__ inline SmallSmem small_smem(int E, int R) {
   s.rstart = o; o += ((R + 1 + 3) & ~3) * 4;
   s.scr = o;    o += 36 * 4;                       // scan scratch, [33] = errors
   s.own = o;    o += kSmallOwnPairs * 4;           // rows of this CTA's pairs
+  s.rows = o;   o += static_cast<int>(row_bytes);  // staged x rows (16-byte aligned)
   s.bytes = o;
   return s;
 }
+
+// n / d for 0 <= n < 2^16 and 1 <= d <= 2048 by a multiply-high with
+// magic = ceil(2^32 / d) (magic 0 stands for d = 1): the product's error,
+// below n / 2^32 < 2^-16, never reaches the next multiple of 1/d.
+__host__ __device__ inline uint32_t div_magic(uint32_t d) {
+  return d == 1 ? 0u : uint32_t(0xFFFFFFFFu / d + 1u);
+}
+__device__ __forceinline__ int small_div(int n, uint32_t magic) {
+  return magic == 0 ? n : int(__umulhi(uint32_t(n), magic));
+}
+
+// A selection packed for the survey: expert in the low 16 bits, its
+// destination rank in the high 16 (both below 2048), -1 if unused.
+__device__ __forceinline__ int32_t pack_route(int e, uint32_t eg_magic) {
+  return e < 0 ? -1 : (e | (small_div(e, eg_magic) << 16));
+}
+__device__ __forceinline__ int route_expert(int32_t v) { return v < 0 ? -1 : (v & 0xFFFF); }
 
 // CTAs of the one-launch layout (each owns about T / kSmallLayoutCtas tokens).
 constexpr int kSmallLayoutCtas = kLayoutMaxTiles;
@@ -631,9 +658,9 @@ constexpr int kSmallLayoutCtas = kLayoutMaxTiles;
 // bf16 rows (1) or E4M3 rows with row-major 1x128 scales (2) -- the same
 // rows and values as dispatch_bf16_kernel / dispatch_fp8_kernel write.
 template <int kMode>
-__global__ void __launch_bounds__(kLayoutThreads)
+__global__ void __launch_bounds__(kSmallThreads)
     layout_small_kernel(const int64_t* __restrict__ topk_idx, int T, int K, int E,
-                        int R, int A, SmallDispatch d,
+                        int R, int A, SmallDispatch d, int staged,
                         uint8_t* __restrict__ is_token_in_rank,
                         int32_t* __restrict__ expert_count,
                         int32_t* __restrict__ expert_start,
@@ -648,7 +675,10 @@ __global__ void __launch_bounds__(kLayoutThreads)
                         int32_t* __restrict__ err) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int Epad = padded_experts(E), Rpad = padded_ranks(R);
-  const SmallSmem L = small_smem(E, R);
+  const int64_t row_bytes = int64_t(d.H) * (kMode != 0 ? 2 : 0);
+  const int tt = (T + gridDim.x - 1) / gridDim.x;
+  const SmallSmem L = small_smem(E, R, staged ? tt * row_bytes : 0);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
   int32_t* s_idx = reinterpret_cast<int32_t*>(smem + L.idx);      // [T * K]
   int32_t* hist = reinterpret_cast<int32_t*>(smem + L.hist);      // [3][Epad]
   int32_t* s_start = reinterpret_cast<int32_t*>(smem + L.start);
@@ -663,73 +693,82 @@ __global__ void __launch_bounds__(kLayoutThreads)
 
   for (int i = tid; i < 3 * Epad; i += blockDim.x) hist[i] = 0;
   for (int i = tid; i < 3 * Rpad; i += blockDim.x) rcnt[i] = 0;
-  if (tid == 0) s_scr[33] = 0;
+  if (tid == 0) {
+    s_scr[33] = 0;
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
   __syncthreads();
   pdl_wait();
 
   // This CTA's tokens [ctb, cte).
-  const int tt = (T + gridDim.x - 1) / gridDim.x;
   const int ctb = min(T, int(blockIdx.x) * tt), cte = min(T, ctb + tt);
   const int Eg = E / R;
+  const uint32_t eg_magic = div_magic(uint32_t(Eg));
+
+  // Fused dispatch with staged rows: the CTA's own x rows (contiguous) are
+  // bulk-copied into shared memory now, so that their DRAM latency passes
+  // while the layout is computed.
+  const uint32_t stage_bytes = uint32_t((cte - ctb) * row_bytes);
+  if (kMode != 0 && staged && tid == 0 && stage_bytes > 0) {
+    mbar_arrive_expect_tx(bar, stage_bytes);
+    bulk_load(smem + L.rows, reinterpret_cast<const uint8_t*>(d.x) + ctb * row_bytes,
+              stage_bytes, bar);
+  }
 
   // The whole input, range-checked (an id outside [-1, E) is reported and
-  // read as -1), in shared memory: one pass of independent loads.  The rank
-  // rows of this CTA's tokens are cleared meanwhile (set per rank below).
+  // read as -1), in shared memory, each selection packed with its
+  // destination rank: one pass of independent loads.  The rank rows of this
+  // CTA's tokens are cleared meanwhile (set per rank below).
   int errbits = 0;
 #pragma unroll 4
-  for (int i = tid; i < T * K; i += blockDim.x) s_idx[i] = read_expert(topk_idx + i, E, errbits);
+  for (int i = tid; i < T * K; i += blockDim.x)
+    s_idx[i] = pack_route(read_expert(topk_idx + i, E, errbits), eg_magic);
   for (int i = tid; i < (cte - ctb) * R; i += blockDim.x)
     is_token_in_rank[int64_t(ctb) * R + i] = 0;
   __syncthreads();
 
-  // Survey in token-aligned warp steps: lanes [0, TPS*K) hold the pairs of
-  // TPS consecutive tokens.  Each lane adds its pair to its region's expert
-  // count, and looks at the earlier selections of its own token (by
-  // shuffles from the token's adjacent lanes): the same expert again is a repeat;
-  // no earlier expert on the same rank makes it the token's first on that
+  // Survey, one pair a thread (thread = (token slot, k), so no division per
+  // pair): the pair adds to its region's expert count (tokens before,
+  // inside and after this CTA's range) and reads its token's earlier
+  // selections from shared memory: the same expert again is a repeat; no
+  // earlier selection on the same rank makes it the token's first on that
   // rank, which adds one to the region's rank count and, for this CTA's own
   // tokens, sets the rank-row flag.
-  {
-    const int TPS = 32 / K, SP = TPS * K;
-    const int steps = (T + TPS - 1) / TPS;
-    const int tl = lane / K, kk = lane - tl * K;
-    const int g0 = tl * K;
-    for (int st = warp; st < steps; st += kLayoutWarps) {
-      const int t = st * TPS + tl;
-      const bool live = lane < SP && t < T;
-      const int e = live ? s_idx[st * SP + lane] : -1;
-      const int r = e >= 0 ? e / Eg : -1;
-      // the token's selections sit in lanes [g0, g0 + K): read them by
-      // shuffles (lanes past the step read wrapped lanes, unused)
-      bool first = true;
-      for (int j = 0; j < K; ++j) {
-        const int ej = __shfl_sync(0xffffffffu, e, (g0 + j) & 31);
-        const int rj = __shfl_sync(0xffffffffu, r, (g0 + j) & 31);
-        if (j < kk && ej >= 0) {
-          if (ej == e) errbits |= ERRBIT_DUP_EXPERT;
-          if (rj == r) first = false;
-        }
-      }
-      if (e < 0) continue;
-      const int region = t < ctb ? 0 : (t < cte ? 1 : 2);
-      atomicAdd(&hist[region * Epad + e], 1);
-      if (first) {
-        atomicAdd(&rcnt[region * Rpad + r], 1);
-        if (region == 1) is_token_in_rank[int64_t(t) * R + r] = 1;
-      }
+  const int tps = blockDim.x / K;               // tokens per pass
+  const int sv_t = tid / K, sv_k = tid - sv_t * K;
+  for (int t = sv_t; sv_t < tps && t < T; t += tps) {
+    const int32_t* tok = s_idx + t * K;
+    const int32_t v = tok[sv_k];
+    if (v < 0) continue;
+    bool first = true;
+    for (int j = 0; j < sv_k; ++j) {
+      const int32_t u = tok[j];
+      if (u < 0) continue;
+      if (u == v) errbits |= ERRBIT_DUP_EXPERT;
+      if ((u >> 16) == (v >> 16)) first = false;
+    }
+    const int e = v & 0xFFFF, r = v >> 16;
+    const int region = t < ctb ? 0 : (t < cte ? 1 : 2);
+    atomicAdd(&hist[region * Epad + e], 1);
+    if (first) {
+      atomicAdd(&rcnt[region * Rpad + r], 1);
+      if (region == 1) is_token_in_rank[int64_t(t) * R + r] = 1;
     }
   }
   if (errbits) atomicOr(&s_scr[33], errbits);
   __syncthreads();
 
-  // Per-expert totals, then the aligned exclusive scan over experts.
-  for (int e = tid; e < E; e += blockDim.x)
-    s_total[e] = hist[e] + hist[Epad + e] + hist[2 * Epad + e];
-  __syncthreads();
+  // Per-expert totals and the aligned exclusive scan over experts (each
+  // thread sums the three regions of its own experts).
   const int per = (E + blockDim.x - 1) / blockDim.x;
   const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
   int local = 0;
-  for (int e = e0; e < e1; ++e) local += (s_total[e] + A - 1) / A * A;
+  for (int e = e0; e < e1; ++e) {
+    const int c = hist[e] + hist[Epad + e] + hist[2 * Epad + e];
+    s_total[e] = c;
+    local += (c + A - 1) / A * A;
+  }
   int used = 0;
   int run = block_exclusive_scan(local, s_scr, &used);
   for (int e = e0; e < e1; ++e) {
@@ -747,7 +786,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
     const uint32_t lt = lanemask_lt();
     for (int b0 = 0; b0 < pe; b0 += 32) {
       const int p = b0 + lane;
-      const int e = p < pe ? src[p] : -1;
+      const int e = p < pe ? route_expert(src[p]) : -1;
       const uint32_t peers = __match_any_sync(0xffffffffu, e);
       int slot = -1;
       if (e >= 0) slot = s_base[e] + __popc(peers & lt);
@@ -805,7 +844,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
       for (int q = tid; q <= R; q += blockDim.x) rank_row_start[q] = s_rstart[q];
     const int nt = cte - ctb;
     const uint32_t lt = lanemask_lt();
-    for (int q = warp; q < R; q += kLayoutWarps) {
+    for (int q = warp; q < R; q += kSmallWarps) {
       int rr = s_rstart[q] + rcnt[q];
       for (int c0 = 0; c0 < nt; c0 += 32) {
         const int t = ctb + c0 + lane;
@@ -821,22 +860,39 @@ __global__ void __launch_bounds__(kLayoutThreads)
   }
 
   // Alignment padding rows carry no token (one warp per expert at a time).
-  for (int e = blockIdx.x * kLayoutWarps + warp; e < E; e += gridDim.x * kLayoutWarps) {
+  for (int e = blockIdx.x * kSmallWarps + warp; e < E; e += gridDim.x * kSmallWarps) {
     const int s0 = s_start[e] + s_total[e], s1 = s_start[e + 1];
     for (int s = s0 + lane; s < s1; s += 32) src_info2[s] = make_int2(-1, -1);
   }
 
   if (kMode == 0) return;
-  // Dispatch of this CTA's own tokens to the rows just assigned.
-  __syncthreads();
+  // Dispatch of this CTA's own tokens to the rows just assigned, from the
+  // staged rows in shared memory (or from x when they did not fit).
+  if (staged && stage_bytes > 0) {
+    if (tid == 0) s_scr[32] = mbar_wait(bar, 0, kWaitTimeoutNs);
+    __syncthreads();
+    if (!s_scr[32]) {
+      // the copy did not land in time: report, wait (bounded) once more for
+      // it to finish, and leave without dispatching
+      if (tid == 0) {
+        record_error(err, ERRBIT_TIMEOUT);
+        if (!mbar_wait(bar, 0, kWaitTimeoutNs)) record_error(err, ERRBIT_TIMEOUT_PENDING);
+      }
+      return;
+    }
+  } else {
+    __syncthreads();
+  }
   const int nt = cte - ctb;
   const int nvec = d.H >> 3;
+  const uint4* srows = reinterpret_cast<const uint4*>(smem + L.rows);  // staged rows
   if (kMode == 1) {
     uint4* rx = static_cast<uint4*>(d.recv_x);
     for (int i = 0; i < nt; ++i) {
       const uint4* row = d.x + int64_t(ctb + i) * nvec;
+      const uint4* srow = srows + int64_t(i) * nvec;
       for (int v = tid; v < nvec; v += blockDim.x) {
-        const uint4 r = ld_stream_u4(row + v);
+        const uint4 r = staged ? srow[v] : ld_stream_u4(row + v);
         for (int k = 0; k < K; ++k) {
           const int sl = s_own[i * K + k];
           if (sl >= 0) rx[int64_t(sl) * nvec + v] = r;
@@ -849,13 +905,19 @@ __global__ void __launch_bounds__(kLayoutThreads)
     const int n16 = d.H >> 4, nblk = d.H >> 7;
     for (int i = 0; i < nt; ++i) {
       const uint4* row = d.x + int64_t(ctb + i) * nvec;
+      const uint4* srow = srows + int64_t(i) * nvec;
       for (int base = 0; base < n16; base += blockDim.x) {
         const int u = base + tid;
         const bool active = u < n16;
         uint4 r0 = make_uint4(0, 0, 0, 0), r1 = r0;
         if (active) {
-          r0 = ld_stream_u4(row + 2 * u);
-          r1 = ld_stream_u4(row + 2 * u + 1);
+          if (staged) {
+            r0 = srow[2 * u];
+            r1 = srow[2 * u + 1];
+          } else {
+            r0 = ld_stream_u4(row + 2 * u);
+            r1 = ld_stream_u4(row + 2 * u + 1);
+          }
         }
         uint4 q;
         float scale;
@@ -901,9 +963,9 @@ int assign_grid(int tiles, int E) {
 
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
   if (layout_is_small(a.T, a.K, a.E)) {
-    return launch_pdl(layout_small_kernel<0>, dim3(kSmallLayoutCtas), dim3(kLayoutThreads),
+    return launch_pdl(layout_small_kernel<0>, dim3(kSmallLayoutCtas), dim3(kSmallThreads),
                       small_smem(a.E, a.R).bytes, stream, a.topk_idx, a.T, a.K, a.E, a.R,
-                      a.A, SmallDispatch{}, a.is_token_in_rank, a.expert_count, a.expert_start,
+                      a.A, SmallDispatch{}, 0, a.is_token_in_rank, a.expert_count, a.expert_start,
                       a.expert_end, a.rank_start, a.tokens_per_rank, a.slot_of, a.src_info,
                       a.rank_row_start, a.rank_slot_of, a.rank_src, a.err);
   }
@@ -921,7 +983,7 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
   // layout (zero counts and offsets).
   const AssignSmem sm = assign_smem(a.E, a.R, tiles);
   const int grid = assign_grid(tiles, a.E);
-  return launch_pdl(layout_assign_kernel, dim3(grid), dim3(kLayoutThreads),
+  return launch_pdl(layout_assign_kernel, dim3(grid), dim3(kAssignThreads),
                     sm.bytes, stream, a.topk_idx, a.T, a.K, a.E, a.R, a.A, tt,
                     tiles, a.ws.tile_counts, a.ws.tile_err,
                     static_cast<const uint8_t*>(a.is_token_in_rank), a.expert_count,
@@ -952,9 +1014,16 @@ cudaError_t launch_layout_dispatch(const LayoutArgs& la, const DispatchArgs& da,
   d.recv_w = da.recv_w;
   d.H = da.H;
   auto kern = da.fp8 ? layout_small_kernel<2> : layout_small_kernel<1>;
-  cudaError_t st = launch_pdl(kern, dim3(kSmallLayoutCtas), dim3(kLayoutThreads),
-                              small_smem(la.E, la.R).bytes, stream, la.topk_idx, la.T, la.K,
-                              la.E, la.R, la.A, d, la.is_token_in_rank, la.expert_count,
+  // Stage the CTAs' own x rows in shared memory when they fit beside the
+  // layout's arrays.
+  const int tt = (la.T + kSmallLayoutCtas - 1) / kSmallLayoutCtas;
+  const int64_t staged_bytes = small_smem(la.E, la.R, int64_t(tt) * da.H * 2).bytes;
+  const bool staged = staged_bytes <= kSmallStageBudget &&
+                      (reinterpret_cast<uintptr_t>(da.x) & 15) == 0;
+  const int smem = staged ? int(staged_bytes) : small_smem(la.E, la.R).bytes;
+  cudaError_t st = launch_pdl(kern, dim3(kSmallLayoutCtas), dim3(kSmallThreads),
+                              smem, stream, la.topk_idx, la.T, la.K,
+                              la.E, la.R, la.A, d, int(staged), la.is_token_in_rank, la.expert_count,
                               la.expert_start, la.expert_end, la.rank_start,
                               la.tokens_per_rank, la.slot_of, la.src_info, la.rank_row_start,
                               la.rank_slot_of, la.rank_src, la.err);
