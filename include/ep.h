@@ -148,7 +148,8 @@ EP_API int64_t ep_layout_workspace_bytes(const ep_config *cfg);
  * source-global order (source rank, token, k) -- the pages' deterministic
  * mode, produced directly.  Logical source ranks own contiguous token
  * blocks, so that order is (t, k) order.  Runs one kernel on `stream` when
- * num_tokens * K <= 4096, else two.
+ * num_tokens * K <= 4096, else two.  The layout's error word is cleared by
+ * the call itself before anything is recorded in it.
  *
  * h_expert_count: NULL for a fully asynchronous call.  If non-NULL (host
  * memory, E int32), the call synchronises `stream`, copies the per-expert
@@ -209,11 +210,14 @@ EP_API int32_t ep_combine(const ep_config *cfg, const ep_layout *layout,
  * followed by ep_dispatch of the same num_tokens tokens, and the same errors
  * for the same arguments.  For inputs of at most 4096 (t, k) pairs whose
  * one-launch layout gives each of its CTAs at most 64 pairs, one kernel does
- * both: each CTA of the layout dispatches its own tokens as soon as their
- * rows are known, so the dispatch costs no second launch.  Larger inputs
- * run the two paths in turn.  (Column-major scales and pre-quantised input
- * are ep_dispatch_fp8's and are not offered here.)  Returns EP_OK or an
- * error. */
+ * both: each CTA of the layout copies the x rows of its own tokens into
+ * shared memory while it computes the layout (when they fit beside its
+ * other arrays), then dispatches them as soon as their rows are known, so
+ * the dispatch costs no second launch.  Larger inputs run the two paths in
+ * turn.  (Column-major scales and pre-quantised input are ep_dispatch_fp8's
+ * and are not offered here.)  If the copy of the staged rows were to give
+ * up its bounded wait, the error word records EP_ERR_TIMEOUT and those
+ * rows are not dispatched.  Returns EP_OK or an error. */
 EP_API int32_t ep_layout_and_dispatch(const ep_config *cfg, int32_t num_tokens,
                                       const int64_t *d_topk_idx, ep_layout *layout,
                                       const void *d_x, const float *d_topk_weights,
