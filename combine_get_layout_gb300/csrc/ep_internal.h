@@ -22,10 +22,10 @@ constexpr int kLayoutMaxTiles = 152;
 constexpr int kMinTilePairs = 256;
 // The assign kernel loads the whole tile-count matrix with one bulk copy
 // when it fits, with the kernel's other shared arrays, in kAssignSmemBudget
-// bytes; otherwise it streams it through two buffers of kScanChunkInts
-// entries.
+// bytes; otherwise it streams it through two buffers of about
+// kScanChunkBytes.
 constexpr int kAssignSmemBudget = 220 * 1024;
-constexpr int kScanChunkInts = 8192;
+constexpr int kScanChunkBytes = 32 * 1024;
 // Inputs of at most kSmallLayoutPairs (t, k) pairs, with at most
 // kSmallLayoutMaxExperts experts, take the one-launch layout.
 constexpr int kSmallLayoutPairs = 4096;
@@ -61,9 +61,21 @@ __host__ __device__ inline int count_row_width(int E, int R) {
   return padded_experts(E) + padded_ranks(R);
 }
 
-// Workspace carved by ep_get_layout (int32 arrays, each 16-byte aligned):
-//   tile_counts [kLayoutMaxTiles * (Epad + Rpad)] (row c: tile c's expert
-//   counts, then its rank counts), tile_err [kLayoutMaxTiles].
+// Entries of a tile-count row as the count kernel stores it: 32-bit
+// counts, or 16-bit counts (when a tile holds at most 65535 (t, k) pairs)
+// with the row rounded up to 8 entries so that it stays a 16-byte multiple.
+__host__ __device__ inline int count_row_entries(int E, int R, bool k16) {
+  const int Wc = count_row_width(E, R);
+  return k16 ? (Wc + 7) & ~7 : Wc;
+}
+__host__ __device__ inline int count_row_bytes(int E, int R, bool k16) {
+  return count_row_entries(E, R, k16) * (k16 ? 2 : 4);
+}
+
+// Workspace carved by ep_get_layout (arrays 16-byte aligned):
+//   tile_counts: kLayoutMaxTiles rows of count_row_bytes (row c: tile c's
+//   expert counts, then its rank counts; sized for 32-bit counts, the
+//   16-bit form uses part of it), tile_err [kLayoutMaxTiles] int32.
 struct LayoutWorkspace {
   int32_t* tile_counts;
   int32_t* tile_err;

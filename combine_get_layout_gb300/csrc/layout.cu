@@ -164,6 +164,7 @@ __device__ __forceinline__ void survey_span(const int64_t* __restrict__ src, int
 // ---------------------------------------------------------------------------
 // 1. count
 // ---------------------------------------------------------------------------
+template <bool k16>
 __global__ void __launch_bounds__(kLayoutThreads)
     layout_count_kernel(const int64_t* __restrict__ topk_idx, int T, int K,
                         int E, int R, int tile_tokens,
@@ -201,8 +202,19 @@ __global__ void __launch_bounds__(kLayoutThreads)
   if (bits) atomicOr(&s_err, bits);
   __syncthreads();
 
-  for (int e = tid; e < Wc; e += blockDim.x)
-    tile_counts[int64_t(tile) * Wc + e] = hist[e];
+  if (k16) {
+    // two 16-bit counts a word, the row padded with zeros to 8 entries
+    const int Wr = count_row_entries(E, R, true);
+    uint32_t* row = reinterpret_cast<uint32_t*>(tile_counts) + int64_t(tile) * (Wr / 2);
+    for (int i = tid; i < Wr / 2; i += blockDim.x) {
+      const uint32_t lo = 2 * i < Wc ? uint32_t(hist[2 * i]) : 0u;
+      const uint32_t hi = 2 * i + 1 < Wc ? uint32_t(hist[2 * i + 1]) : 0u;
+      row[i] = lo | (hi << 16);
+    }
+  } else {
+    for (int e = tid; e < Wc; e += blockDim.x)
+      tile_counts[int64_t(tile) * Wc + e] = hist[e];
+  }
   if (tid == 0) tile_err[tile] = s_err;
 }
 
@@ -248,35 +260,38 @@ struct AssignSmem {
 };
 
 // Shared-memory plan of the assign kernel; identical on host and device.
-__host__ __device__ inline AssignSmem assign_smem(int E, int R, int num_tiles) {
+// k16: the tile-count rows hold 16-bit counts (count_row_entries).
+__host__ __device__ inline AssignSmem assign_smem(int E, int R, int num_tiles, bool k16) {
   const int Epad = padded_experts(E), Rpad = padded_ranks(R);
-  const int Wc = Epad + Rpad;
+  const int Wr = count_row_entries(E, R, k16);       // entries a stored row
+  const int row_bytes = count_row_bytes(E, R, k16);
   AssignSmem s;
-  // column sums: 4 columns a thread; the threads left over take row groups
-  // (at most as many as keep the partial sums within 16 KB)
-  const int col_groups = Wc / 4;
+  // column sums: one 16-byte vector of a row a thread (4 or 8 columns); the
+  // threads left over take row groups (at most as many as keep the partial
+  // sums, int32 per column, within 16 KB)
+  const int col_groups = Wr / (k16 ? 8 : 4);
   s.row_groups = col_groups < kAssignThreads ? kAssignThreads / col_groups : 1;
-  const int max_groups = 16384 / (8 * Wc);
+  const int max_groups = 16384 / (8 * Wr);
   if (s.row_groups > max_groups) s.row_groups = max_groups > 1 ? max_groups : 1;
-  const int part_bytes = 2 * s.row_groups * Wc * 4;
+  const int part_bytes = 2 * s.row_groups * Wr * 4;
   // bytes of everything but the count rows (barriers, histograms, scans,
   // partial sums)
   const int other = 16 + kLayoutWarps * E * 4 + ((E + 1 + 3) & ~3) * 4 + 2 * Epad * 4 +
                     ((R + 1 + 3) & ~3) * 4 + 2 * Rpad * 4 + 36 * 4 + part_bytes;
   int rows, nbuf;
-  if (num_tiles >= 1 && other + num_tiles * Wc * 4 <= kAssignSmemBudget) {
+  if (num_tiles >= 1 && other + num_tiles * row_bytes <= kAssignSmemBudget) {
     rows = num_tiles;  // the whole matrix in one bulk copy
     nbuf = 1;
   } else {
-    rows = kScanChunkInts / Wc;
+    rows = kScanChunkBytes / row_bytes;
     if (rows < 1) rows = 1;
     if (num_tiles >= 1 && rows > num_tiles) rows = num_tiles;
     nbuf = 2;
   }
   s.chunk_rows = rows;
   s.bar = 0;                                   // 2 x 8 bytes, padded
-  s.ring = 16;                                 // nbuf x rows x Wc int32
-  s.whist = s.ring + nbuf * rows * Wc * 4;     // kLayoutWarps x E
+  s.ring = 16;                                 // nbuf x rows x row_bytes
+  s.whist = s.ring + nbuf * rows * row_bytes;  // kLayoutWarps x E
   s.start = s.whist + kLayoutWarps * E * 4;    // E + 1
   s.base = s.start + ((E + 1 + 3) & ~3) * 4;   // E
   s.total = s.base + Epad * 4;                 // E
@@ -284,11 +299,12 @@ __host__ __device__ inline AssignSmem assign_smem(int E, int R, int num_tiles) {
   s.rbase = s.rstart + ((R + 1 + 3) & ~3) * 4; // R
   s.rtotal = s.rbase + Rpad * 4;               // R
   s.scratch = s.rtotal + Rpad * 4;             // 32 + 4
-  s.part = s.scratch + 36 * 4;                 // 2 x row_groups x Wc
+  s.part = s.scratch + 36 * 4;                 // 2 x row_groups x Wr int32
   s.bytes = s.part + part_bytes;
   return s;
 }
 
+template <bool k16>
 __global__ void __launch_bounds__(kAssignThreads)
     layout_assign_kernel(const int64_t* __restrict__ topk_idx, int T, int K,
                          int E, int R, int A, int tile_tokens, int num_tiles,
@@ -309,10 +325,11 @@ __global__ void __launch_bounds__(kAssignThreads)
                          uint64_t wait_ns) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int Epad = padded_experts(E);
-  const int Wc = count_row_width(E, R);
-  const AssignSmem L = assign_smem(E, R, num_tiles);
+  const int Wr = count_row_entries(E, R, k16);
+  const int row_bytes = count_row_bytes(E, R, k16);
+  const AssignSmem L = assign_smem(E, R, num_tiles, k16);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
-  int32_t* ring = reinterpret_cast<int32_t*>(smem + L.ring);
+  uint8_t* ring = smem + L.ring;
   int32_t* whist = reinterpret_cast<int32_t*>(smem + L.whist);
   int32_t* s_start = reinterpret_cast<int32_t*>(smem + L.start);
   int32_t* s_base = reinterpret_cast<int32_t*>(smem + L.base);
@@ -356,10 +373,11 @@ __global__ void __launch_bounds__(kAssignThreads)
     if (stall) return;
     const int r0 = ch * rows;
     const int n = min(rows, num_tiles - r0);
-    const uint32_t bytes = uint32_t(n) * uint32_t(Wc) * 4u;
+    const uint32_t bytes = uint32_t(n) * uint32_t(row_bytes);
     mbar_arrive_expect_tx(&bar[ch & 1], bytes);
-    bulk_load(ring + (ch & 1) * rows * Wc, tile_counts + int64_t(r0) * Wc,
-              bytes, &bar[ch & 1]);
+    bulk_load(ring + (ch & 1) * rows * row_bytes,
+              reinterpret_cast<const uint8_t*>(tile_counts) + int64_t(r0) * row_bytes, bytes,
+              &bar[ch & 1]);
     issued = ch + 1;
   };
   if (tid == 0) {
@@ -404,38 +422,63 @@ __global__ void __launch_bounds__(kAssignThreads)
     }
     const int r0 = ch * rows;
     const int n = min(rows, num_tiles - r0);
-    const int32_t* buf = ring + (ch & 1) * rows * Wc;
+    const uint8_t* buf = ring + (ch & 1) * rows * row_bytes;
     // Column sums -- all rows (totals) and rows of earlier tiles (this
-    // tile's base) -- 4 columns a thread with one 16-byte load a row, rows
-    // split into L.row_groups groups so that many loads are in flight; the
-    // groups' partial sums then meet in shared memory.
+    // tile's base) -- one 16-byte vector of each row a thread (4 32-bit or
+    // 8 16-bit counts), rows split into L.row_groups groups so that many
+    // loads are in flight; the groups' partial sums then meet in shared
+    // memory.
     {
       const int nb = min(n, max(0, tile - r0));   // rows of earlier tiles
-      const int col_groups = Wc / 4, G = L.row_groups;
+      constexpr int kCols = k16 ? 8 : 4;          // columns a vector
+      const int col_groups = Wr / kCols, G = L.row_groups;
       const int per = (n + G - 1) / G;
       for (int w = tid; w < col_groups * G; w += blockDim.x) {
         const int cgi = w % col_groups, g = w / col_groups;
         const int ra = g * per, rb = min(n, ra + per);
-        int4 tot = make_int4(0, 0, 0, 0), bas = tot;
+        int tot[kCols], bas[kCols];
+#pragma unroll
+        for (int j = 0; j < kCols; ++j) tot[j] = bas[j] = 0;
 #pragma unroll 4
         for (int r = ra; r < rb; ++r) {
-          const int4 v = *reinterpret_cast<const int4*>(buf + r * Wc + cgi * 4);
-          tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
+          const uint4 v = *reinterpret_cast<const uint4*>(buf + r * row_bytes + cgi * 16);
+          int c[kCols];
+          if constexpr (k16) {
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              c[2 * q] = int(wv[q] & 0xFFFFu);
+              c[2 * q + 1] = int(wv[q] >> 16);
+            }
+          } else {
+            c[0] = int(v.x);
+            c[1] = int(v.y);
+            c[2] = int(v.z);
+            c[3] = int(v.w);
+          }
+#pragma unroll
+          for (int j = 0; j < kCols; ++j) tot[j] += c[j];
           if (r < nb) {
-            bas.x += v.x; bas.y += v.y; bas.z += v.z; bas.w += v.w;
+#pragma unroll
+            for (int j = 0; j < kCols; ++j) bas[j] += c[j];
           }
         }
-        *reinterpret_cast<int4*>(s_part + (g * Wc + cgi * 4)) = tot;
-        *reinterpret_cast<int4*>(s_part + ((G + g) * Wc + cgi * 4)) = bas;
+#pragma unroll
+        for (int j = 0; j < kCols; j += 4) {
+          *reinterpret_cast<int4*>(s_part + (g * Wr + cgi * kCols + j)) =
+              make_int4(tot[j], tot[j + 1], tot[j + 2], tot[j + 3]);
+          *reinterpret_cast<int4*>(s_part + ((G + g) * Wr + cgi * kCols + j)) =
+              make_int4(bas[j], bas[j + 1], bas[j + 2], bas[j + 3]);
+        }
       }
       __syncthreads();
-      for (int c = tid; c < Wc; c += blockDim.x) {
+      for (int c = tid; c < Wr; c += blockDim.x) {
         const bool is_e = c < E, is_r = c >= Epad && c - Epad < R;
         if (!is_e && !is_r) continue;
         int tot = 0, bas = 0;
         for (int g = 0; g < G; ++g) {
-          tot += s_part[g * Wc + c];
-          bas += s_part[(G + g) * Wc + c];
+          tot += s_part[g * Wr + c];
+          bas += s_part[(G + g) * Wr + c];
         }
         if (is_e) {
           s_base[c] += bas;
@@ -942,12 +985,14 @@ static int count_smem(int E, int R, int K) {
 
 cudaError_t prepare_layout_kernels() {
   const int optin = device_info().max_smem_optin;
-  cudaError_t st = allow_max_dynamic_smem(layout_count_kernel, optin);
+  cudaError_t st = allow_max_dynamic_smem(layout_count_kernel<false>, optin);
+  if (st == cudaSuccess) st = allow_max_dynamic_smem(layout_count_kernel<true>, optin);
   if (st == cudaSuccess) st = allow_max_dynamic_smem(layout_small_kernel<0>, optin);
   if (st == cudaSuccess) st = allow_max_dynamic_smem(layout_small_kernel<1>, optin);
   if (st == cudaSuccess) st = allow_max_dynamic_smem(layout_small_kernel<2>, optin);
+  if (st == cudaSuccess) st = allow_max_dynamic_smem(layout_assign_kernel<false>, optin);
   if (st != cudaSuccess) return st;
-  return allow_max_dynamic_smem(layout_assign_kernel, optin);
+  return allow_max_dynamic_smem(layout_assign_kernel<true>, optin);
 }
 
 bool layout_is_small(int64_t T, int K, int E) {
@@ -971,19 +1016,22 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
   }
   const int tiles = a.T > 0 ? a.geom.num_tiles : 0;
   const int tt = a.geom.tile_tokens;
+  // 16-bit tile counts when no count can exceed them (a tile's pairs)
+  const bool k16 = int64_t(tt) * a.K <= 0xFFFF;
   cudaError_t st;
   if (tiles > 0) {
-    st = launch_pdl(layout_count_kernel, dim3(tiles), dim3(kLayoutThreads),
-                    count_smem(a.E, a.R, a.K), stream, a.topk_idx, a.T, a.K,
-                    a.E, a.R, tt, a.ws.tile_counts, a.ws.tile_err,
-                    a.is_token_in_rank, a.err);
+    st = launch_pdl(k16 ? layout_count_kernel<true> : layout_count_kernel<false>, dim3(tiles),
+                    dim3(kLayoutThreads), count_smem(a.E, a.R, a.K), stream, a.topk_idx, a.T,
+                    a.K, a.E, a.R, tt, a.ws.tile_counts, a.ws.tile_err, a.is_token_in_rank,
+                    a.err);
     if (st != cudaSuccess) return st;
   }
   // With no tokens there are no tiles: one CTA still publishes the empty
   // layout (zero counts and offsets).
-  const AssignSmem sm = assign_smem(a.E, a.R, tiles);
+  const AssignSmem sm = assign_smem(a.E, a.R, tiles, k16);
   const int grid = assign_grid(tiles, a.E);
-  return launch_pdl(layout_assign_kernel, dim3(grid), dim3(kAssignThreads),
+  return launch_pdl(k16 ? layout_assign_kernel<true> : layout_assign_kernel<false>, dim3(grid),
+                    dim3(kAssignThreads),
                     sm.bytes, stream, a.topk_idx, a.T, a.K, a.E, a.R, a.A, tt,
                     tiles, a.ws.tile_counts, a.ws.tile_err,
                     static_cast<const uint8_t*>(a.is_token_in_rank), a.expert_count,

@@ -168,6 +168,28 @@ def test_layout_more_tiles_than_target(ep):
     assert_layout_equal(L, oracle_layout(wl, idx, cfg.capacity), wl.num_tokens)
 
 
+@pytest.mark.parametrize("T,K,E,R", [
+    # 152 tiles of exactly 65535 pairs, every pair on one expert: each
+    # tile's count is the largest a 16-bit count holds
+    (152 * 65535, 1, 1, 1),
+    # tiles of 68,424 pairs: past 16-bit counts, the 32-bit rows
+    (1_300_000, 8, 64, 8),
+])
+def test_layout_tile_count_width_edges(ep, T, K, E, R):
+    wl = workloads.Workload("edge", T, 8, E, K, R, False, expert_alignment=4)
+    if E == 1:
+        idx = np.zeros((T, 1), np.int64)
+    else:
+        rng = np.random.default_rng(15)
+        idx = np.empty((T, K), np.int64)
+        for c0 in range(0, T, 100_000):           # distinct experts per token
+            n = min(100_000, T - c0)
+            idx[c0:c0 + n] = np.argsort(rng.random((n, E)), axis=1)[:, :K]
+    cfg = cfg_of(ep, wl)
+    L = run_layout(ep, cfg, idx)
+    assert_layout_equal(L, oracle_layout(wl, idx, cfg.capacity), T)
+
+
 @pytest.mark.parametrize("T", [5000, 1000])
 def test_layout_hot_expert(ep, T):
     """Every token picks expert 0 plus others: one expert holds T rows (both
