@@ -1,8 +1,8 @@
 // extern "C" entry points of libep_gb300.so (declared in include/ep.h):
 // host-side validation, sizing, and launches on the caller's stream.  The
 // library holds no state besides a per-device property cache and, once the
-// host-buffer entry points have run on a device, that device's copy stream
-// and events.
+// host-buffer entry points have copied in chunks on a device, that device's
+// two copy streams (one a direction) and their events.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -283,11 +283,18 @@ int32_t ep_combine(const ep_config* cfg, const ep_layout* layout,
 // ---------------------------------------------------------------------------
 constexpr int kMaxHostChunks = 64;
 
-// One copy stream and kMaxHostChunks + 1 events per device, created by the
-// first host-buffer call on the device and kept until exit.
-struct HostIo {
+// Per device and per copy direction (host to device for
+// ep_dispatch_from_host, device to host for ep_combine_to_host): one copy
+// stream and kMaxHostChunks + 1 events, created by the first host-buffer
+// call on the device and kept until exit.  With a stream per direction, a
+// combine's rows going out and the next batch's rows coming in (two calls on
+// two streams) run on the two copy engines at once.
+struct HostIoLane {
   cudaStream_t copy = nullptr;
   cudaEvent_t ev[kMaxHostChunks + 1] = {};
+};
+struct HostIo {
+  HostIoLane h2d, d2h;
 };
 
 static cudaError_t host_io(HostIo** out) {
@@ -297,10 +304,12 @@ static cudaError_t host_io(HostIo** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
   std::call_once(once[dev], [dev] {
-    HostIo& h = io[dev];
-    cudaError_t e = cudaStreamCreateWithFlags(&h.copy, cudaStreamNonBlocking);
-    for (int i = 0; e == cudaSuccess && i <= kMaxHostChunks; ++i)
-      e = cudaEventCreateWithFlags(&h.ev[i], cudaEventDisableTiming);
+    cudaError_t e = cudaSuccess;
+    for (HostIoLane* lane : {&io[dev].h2d, &io[dev].d2h}) {
+      if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&lane->copy, cudaStreamNonBlocking);
+      for (int i = 0; e == cudaSuccess && i <= kMaxHostChunks; ++i)
+        e = cudaEventCreateWithFlags(&lane->ev[i], cudaEventDisableTiming);
+    }
     result[dev] = e;
   });
   *out = &io[dev];
@@ -391,18 +400,19 @@ int32_t ep_dispatch_from_host(const ep_config* cfg, const ep_layout* layout,
   } else if (T > 0) {
     const int n_chunks = (T + tc - 1) / tc;
     // the staging rows are free once the stream's earlier work is done
-    e = cudaEventRecord(io->ev[kMaxHostChunks], s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(io->copy, io->ev[kMaxHostChunks], 0);
+    HostIoLane* io_in = &io->h2d;
+    e = cudaEventRecord(io_in->ev[kMaxHostChunks], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(io_in->copy, io_in->ev[kMaxHostChunks], 0);
     for (int c = 0; e == cudaSuccess && c < n_chunks; ++c) {
       const int t0 = c * tc, n = T - t0 < tc ? T - t0 : tc;
       e = cudaMemcpyAsync(static_cast<char*>(d_x) + t0 * row_bytes,
                           static_cast<const char*>(h_x) + t0 * row_bytes, n * row_bytes,
-                          cudaMemcpyHostToDevice, io->copy);
-      if (e == cudaSuccess) e = cudaEventRecord(io->ev[c], io->copy);
+                          cudaMemcpyHostToDevice, io_in->copy);
+      if (e == cudaSuccess) e = cudaEventRecord(io_in->ev[c], io_in->copy);
     }
     for (int c = 0; e == cudaSuccess && c < n_chunks; ++c) {
       const int t0 = c * tc, n = T - t0 < tc ? T - t0 : tc;
-      e = cudaStreamWaitEvent(s, io->ev[c], 0);
+      e = cudaStreamWaitEvent(s, io_in->ev[c], 0);
       if (e != cudaSuccess) break;
       DispatchArgs a = base;
       a.x = static_cast<const char*>(d_x) + t0 * row_bytes;
@@ -453,6 +463,7 @@ int32_t ep_combine_to_host(const ep_config* cfg, const ep_layout* layout,
   }
   HostIo* io = nullptr;
   if (host_io(&io) != cudaSuccess) return EP_ERR_CUDA;
+  HostIoLane* io_out = &io->d2h;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int K = cfg->num_topk;
   const int64_t row_bytes = int64_t(cfg->hidden) * 2;
@@ -486,16 +497,16 @@ int32_t ep_combine_to_host(const ep_config* cfg, const ep_layout* layout,
     a.y = static_cast<char*>(d_y) + t0 * row_bytes;
     a.pdl = false;
     e = launch_combine(a, s);
-    if (e == cudaSuccess) e = cudaEventRecord(io->ev[c], s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(io->copy, io->ev[c], 0);
+    if (e == cudaSuccess) e = cudaEventRecord(io_out->ev[c], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(io_out->copy, io_out->ev[c], 0);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(static_cast<char*>(h_y) + t0 * row_bytes,
                           static_cast<const char*>(d_y) + t0 * row_bytes, n * row_bytes,
-                          cudaMemcpyDeviceToHost, io->copy);
+                          cudaMemcpyDeviceToHost, io_out->copy);
   }
   // the caller's stream completes only after the last rows reached the host
-  if (e == cudaSuccess) e = cudaEventRecord(io->ev[kMaxHostChunks], io->copy);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, io->ev[kMaxHostChunks], 0);
+  if (e == cudaSuccess) e = cudaEventRecord(io_out->ev[kMaxHostChunks], io_out->copy);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, io_out->ev[kMaxHostChunks], 0);
   return cuda_status(e);
 }
 

@@ -28,9 +28,9 @@
  *  - Pointers named d_* or documented "device" are CUDA device pointers; all
  *    buffers are allocated and owned by the CALLER.  The library never
  *    allocates or frees memory and keeps no pointer after a call returns.
- *    (The host-buffer entry points, when they copy in chunks, create one
- *    copy stream and a few events per device on first use, kept until
- *    exit.)
+ *    (The host-buffer entry points, when they copy in chunks, create two
+ *    copy streams -- one a direction -- and a few events per device on
+ *    first use, kept until exit.)
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Work is enqueued asynchronously on it; a call returns before
  *    the GPU has finished unless documented otherwise.
@@ -412,10 +412,15 @@ EP_API int32_t ep_combine_ranks(const ep_config *cfg, const ep_layout *layout,
  *    bytes split into n = min(num_chunks, max(1, floor(2HT / 4 MiB)))
  *    chunks of ceil(T / n) tokens, the last ragged); a single chunk is
  *    copied on `stream` itself, with no copy stream involved.  The first
- *    chunked call on a device creates that device's copy stream and events
- *    (kept until exit); calls on one device share them, so their copies run
- *    in call order.  Host buffers should be pinned (page-locked): pageable
- *    memory works but its copies do not overlap. */
+ *    chunked call on a device creates that device's two copy streams, one
+ *    for rows coming in (ep_dispatch_from_host) and one for rows going out
+ *    (ep_combine_to_host), and their events (kept until exit).  Calls of
+ *    one direction on one device share its stream, so their copies run in
+ *    call order; the two directions run at once, so a combine's rows going
+ *    out can overlap the next batch's rows coming in when the two calls
+ *    are on different streams.  Calls are made from one host thread at a
+ *    time.  Host buffers should be pinned (page-locked): pageable memory
+ *    works but its copies do not overlap. */
 
 /* As ep_dispatch with x in host memory (h_x: host bf16 [T, H]).  Direct
  * (num_chunks = 0): the dispatch kernel reads h_x in place; d_x is unused.
