@@ -83,7 +83,7 @@ def parse_args():
                         "combine backward (with gate gradients), dispatch backward; "
                         "ranks: layout, dispatch to ranks, expand, reduce to ranks, "
                         "combine over ranks (the non-expanded path)")
-    p.add_argument("--e2e-chunks", type=int, default=8,
+    p.add_argument("--e2e-chunks", type=int, default=4,
                    help="token chunks of the host-buffer entry points in the e2e leg "
                         "when they copy (copies of later chunks overlap the kernels of "
                         "earlier ones)")
@@ -93,8 +93,10 @@ def parse_args():
                         "host memory in place (host-buffer entry points, 0 chunks); "
                         "chunked = the same entry points copying token chunks; copies = "
                         "whole-buffer copies on the stream around the device entry points; "
-                        "auto = direct (copies with the combine epilogue or FP8 input "
-                        "options, which have device entry points only)")
+                        "auto = direct one step at a time, and for two batches in flight "
+                        "chunked when a batch's rows span two 4 MiB chunks, else direct "
+                        "(copies with the combine epilogue or FP8 input options, which have "
+                        "device entry points only; those run one step at a time)")
     p.add_argument("--fused", action="store_true",
                    help="forward pass: layout and dispatch through ep_layout_and_dispatch "
                         "(one kernel for small inputs)")
@@ -425,6 +427,23 @@ def e2e_transfer(requested: str, device_entry_points_only: bool) -> str:
     return "direct" if requested == "auto" else requested
 
 
+def pipelined_transfer(requested: str, device_entry_points_only: bool, row_bytes: int) -> str:
+    """How the pipelined e2e leg (two batches in flight) moves x and y, or
+    None where it does not run (options that only the device entry points
+    offer).  "auto": the host-buffer entry points copying token chunks when
+    a batch's rows span at least two 4 MiB chunks -- then one batch's rows
+    going out and the next batch's coming in use the two copy engines at
+    once -- else direct (small batches: the kernels read and write the host
+    rows in place)."""
+    if requested not in ("auto", "direct", "chunked", "copies"):
+        raise ValueError(f"unknown e2e transfer {requested!r}")
+    if device_entry_points_only:
+        return None
+    if requested != "auto":
+        return requested
+    return "chunked" if row_bytes >= 2 * (4 << 20) else "direct"
+
+
 def path_dtype(wl) -> str:
     """The arithmetic of the path: E4M3 rows (fp32 quantisation) or bf16 bit
     copies on dispatch; the combine folds bf16 rows in fp32 either way."""
@@ -432,15 +451,18 @@ def path_dtype(wl) -> str:
 
 
 def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, idx_h, w_h, recv_x0, Y_d,
-                  chunks, steps, warmup, world, y_want):
+                  chunks, steps, warmup, world, y_want, copies=False):
     """End to end with two batches in flight, as a serving loop runs: step i
     goes on stream i % 2 with its own device buffers and host output rows,
     so one step's combine (y over the host link to the host) overlaps the
     next step's layout and dispatch (x over the link to the device).  Every
     step copies its routes and weights in, reads x from and writes y to
-    pinned host memory through the host-buffer entry points.  No L2 flush:
-    a step touches far more HBM than L2 holds.  Returns the throughput over
-    `steps` steps (one event pair around all of them)."""
+    pinned host memory through the host-buffer entry points (copies=True:
+    copies x to the device and y back itself, on the step's stream, around
+    ep_dispatch / ep_combine on device buffers, so that the two copy
+    directions run on their own copy engines).  No L2 flush: a step touches
+    far more HBM than L2 holds.  Returns the throughput over `steps` steps
+    (one event pair around all of them)."""
     import ctypes
 
     import torch
@@ -464,8 +486,9 @@ def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, idx_h, w_h, r
         sl.rs = (torch.empty((cap, H // 128), dtype=torch.float32, device=device)
                  if wl.use_fp8_dispatch else None)
         sl.rw = torch.empty(cap, dtype=torch.float32, device=device)
-        sl.x_d = torch.empty((T, H), dtype=torch.bfloat16, device=device) if chunks else None
-        sl.y_d = torch.empty((T, H), dtype=torch.bfloat16, device=device) if chunks else None
+        staged = chunks or copies
+        sl.x_d = torch.empty((T, H), dtype=torch.bfloat16, device=device) if staged else None
+        sl.y_d = torch.empty((T, H), dtype=torch.bfloat16, device=device) if staged else None
         sl.y_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
         # experts: identity for bf16 rows, the seeded expert-output buffer for E4M3
         sl.ident = sl.rx if recv_x0 is not None else Y_d
@@ -473,16 +496,28 @@ def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, idx_h, w_h, r
 
     def step(sl):
         with torch.cuda.stream(sl.stream):
+            if copies:
+                sl.x_d.copy_(x_h, non_blocking=True)
             sl.idx.copy_(idx_h, non_blocking=True)
             sl.w.copy_(w_h, non_blocking=True)
         st = ep.ep_get_layout(ccfg, T, p(sl.idx), sl.L.c, None, sl.sptr)
         assert st == 0, ep.ep_status_str(st)
-        st = ep.ep_dispatch_from_host(ccfg, sl.L.c, x_h.data_ptr(), p(sl.x_d), p(sl.w), p(sl.rx),
-                                      p(sl.rs), p(sl.rw), chunks, sl.sptr)
+        if copies:
+            st = ep.ep_dispatch(ccfg, sl.L.c, p(sl.x_d), p(sl.w), p(sl.rx), p(sl.rs), p(sl.rw),
+                                sl.sptr)
+        else:
+            st = ep.ep_dispatch_from_host(ccfg, sl.L.c, x_h.data_ptr(), p(sl.x_d), p(sl.w),
+                                          p(sl.rx), p(sl.rs), p(sl.rw), chunks, sl.sptr)
         assert st == 0, ep.ep_status_str(st)
-        st = ep.ep_combine_to_host(ccfg, sl.L.c, p(sl.ident), p(sl.w), p(sl.y_d), sl.y_h.data_ptr(),
-                                   chunks, sl.sptr)
-        assert st == 0, ep.ep_status_str(st)
+        if copies:
+            st = ep.ep_combine(ccfg, sl.L.c, p(sl.ident), p(sl.w), p(sl.y_d), sl.sptr)
+            assert st == 0, ep.ep_status_str(st)
+            with torch.cuda.stream(sl.stream):
+                sl.y_h.copy_(sl.y_d, non_blocking=True)
+        else:
+            st = ep.ep_combine_to_host(ccfg, sl.L.c, p(sl.ident), p(sl.w), p(sl.y_d),
+                                       sl.y_h.data_ptr(), chunks, sl.sptr)
+            assert st == 0, ep.ep_status_str(st)
 
     def run(n):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -951,10 +986,13 @@ def run_ours(args):
         sequential = {"value": T * world / (e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e_ms,
                       "timing": "one step at a time, L2 flushed before each, events around "
                                 "each step"}
+        p_mode = pipelined_transfer(args.e2e_transfer, bool(epilogue or fp8_opts), T * H * 2)
+        p_chunks = args.e2e_chunks if p_mode == "chunked" else 0
         pipelined = (pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, idx_h, w_h,
-                                   None if wl.use_fp8_dispatch else recv_x, Y_d, chunks,
-                                   args.steps, args.warmup, world, y_h)
-                     if host_io else None)
+                                   None if wl.use_fp8_dispatch else recv_x, Y_d, p_chunks,
+                                   args.steps, args.warmup, world, y_h,
+                                   copies=(p_mode == "copies"))
+                     if p_mode is not None else None)
         e2e = {"unit": "tokens/s",
                "h2d_bytes_per_step": x_h.numel() * 2 + idx_h.numel() * 8 + w_h.numel() * 4,
                "d2h_bytes_per_step": y_h.numel() * 2,
@@ -971,6 +1009,13 @@ def run_ours(args):
         if pipelined is not None:
             e2e.update(value=pipelined["value"], ms_per_step=pipelined["ms_per_step"],
                        pipelining=pipelined["pipelining"])
+            e2e["sequential"]["transfer"] = e2e["transfer"]
+            e2e["transfer"] = (
+                "ep_dispatch_from_host / ep_combine_to_host, direct (the kernels read x and "
+                "write y in pinned host memory)" if p_mode == "direct" else
+                f"ep_dispatch_from_host / ep_combine_to_host, {p_chunks} token chunks on the "
+                "library's copy streams (one a direction)" if p_mode == "chunked" else
+                "whole-buffer copies on each step's stream around ep_dispatch / ep_combine")
         else:
             e2e.update(value=sequential["value"], ms_per_step=e_ms, pipelining=None)
 

@@ -58,3 +58,16 @@ def test_cpu_baseline_reports_all_cores_and_one():
     assert cb["cores"] == bench.host_cores() >= 1
     assert cb["kind"] == "oracle" and cb["unit"] == "tokens/s" and cb["value"] > 0
     assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
+
+
+@pytest.mark.parametrize("requested,device_only,row_bytes,want", [
+    ("auto", False, 4096 * 7168 * 2, "chunked"),    # prefill rows: 58.7 MB
+    ("auto", False, 128 * 7168 * 2, "direct"),      # decode rows: 1.8 MB
+    ("auto", False, 8 << 20, "chunked"),            # exactly two 4 MiB chunks
+    ("auto", False, (8 << 20) - 2, "direct"),
+    ("copies", False, 128, "copies"),
+    ("direct", False, 1 << 30, "direct"),
+    ("auto", True, 1 << 30, None),                  # device entry points only
+])
+def test_pipelined_transfer_choice(requested, device_only, row_bytes, want):
+    assert bench.pipelined_transfer(requested, device_only, row_bytes) == want
