@@ -1,11 +1,13 @@
 """GPU checks of the host-buffer entry points (ep_dispatch_from_host,
 ep_combine_to_host): rows copied in token chunks on the library's copy
-stream, each chunk's kernel waiting for its own copy.  The results must equal
-the device-buffer entry points bit for bit (which the parity suite holds to
-the oracle), for one chunk (on the caller's stream) and several (on the copy
-stream) with a ragged last chunk, FP8 rows and zero padding; one case is
-also compared with the oracle directly.  With 0 chunks (direct) the kernels
-read and write the pinned host rows in place, with no staging buffer."""
+streams (one for host-to-device, one for device-to-host), each chunk's
+kernel waiting for its own copy.  The results must equal the device-buffer
+entry points bit for bit (which the parity suite holds to the oracle), for
+one chunk (on the caller's stream) and several (on the copy streams) with a
+ragged last chunk, FP8 rows and zero padding; one case is also compared with
+the oracle directly, and one keeps two batches in flight on two streams.
+With 0 chunks (direct) the kernels read and write the pinned host rows in
+place, with no staging buffer."""
 
 import mmap
 
@@ -148,6 +150,52 @@ def test_two_calls_in_a_row_reuse_the_events(ep):
         torch.cuda.synchronize()
         assert np.array_equal(u16(h_y), u16(y_ref))
 
+
+
+def test_two_batches_in_flight_on_two_streams(ep):
+    """Two batches, each on its own stream, calls interleaved with no host
+    synchronisation: batch B's rows go up while batch A's results come down,
+    through the same two copy streams.  Every step's y must be its own
+    batch's, bit for bit, and batch A's must match the oracle."""
+    wl = CASES["wide"]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    batches = []
+    for seed, s in zip((2, 3), streams):
+        inp = workloads.make_inputs(wl, seed=seed)
+        cfg = ep.Config(wl.num_tokens, wl.hidden, wl.num_topk, wl.num_experts, wl.num_ranks,
+                        wl.expert_alignment, False, False)
+        idx = dev(inp["topk_idx"])
+        w = dev(inp["topk_weights"])
+        torch.cuda.synchronize()
+        L = ep.get_layout(cfg, idx, sync=True, stream=s)
+        batches.append(dict(inp=inp, cfg=cfg, L=L, w=w, x_h=pinned_bf16(inp["x"]),
+                            s=s, recv=None, d_x=None, d_y=None, ys=[]))
+    steps = 3
+    for _ in range(steps):
+        for b in batches:
+            b["recv"], _, _, b["d_x"] = ep.dispatch_from_host(
+                b["cfg"], b["L"], b["x_h"], d_x=b["d_x"], topk_weights=b["w"],
+                recv_x=b["recv"], num_chunks=5, stream=b["s"])
+        for b in batches:
+            h_y, b["d_y"] = ep.combine_to_host(b["cfg"], b["L"], b["recv"], b["w"],
+                                               d_y=b["d_y"], num_chunks=7, stream=b["s"])
+            b["ys"].append(h_y)
+    for s in streams:
+        s.synchronize()
+    for b in batches:
+        assert ep.check_error(b["L"], stream=b["s"]) == 0
+        recv, _, _ = ep.dispatch(b["cfg"], b["L"], b["x_h"].cuda(), b["w"])
+        y_ref = u16(ep.combine(b["cfg"], b["L"], recv, b["w"]))
+        torch.cuda.synchronize()
+        for h_y in b["ys"]:
+            assert np.array_equal(u16(h_y), y_ref)
+    assert not np.array_equal(u16(batches[0]["ys"][0]), u16(batches[1]["ys"][0]))
+    inp = batches[0]["inp"]
+    ora = oracle.layout(inp["topk_idx"], wl.num_experts, wl.num_ranks, wl.expert_alignment,
+                        cap=batches[0]["cfg"].capacity)
+    rx, _ = oracle.dispatch_bf16(inp["x"], inp["topk_weights"], ora)
+    y_or = oracle.combine(rx, inp["topk_weights"], ora["slot_of"])
+    assert np.array_equal(u16(batches[0]["ys"][-1]), y_or)
 
 def test_empty_batch(ep):
     wl = CASES["few_tokens"]
