@@ -83,10 +83,13 @@ def parse_args():
                         "combine backward (with gate gradients), dispatch backward; "
                         "ranks: layout, dispatch to ranks, expand, reduce to ranks, "
                         "combine over ranks (the non-expanded path)")
-    p.add_argument("--e2e-chunks", type=int, default=4,
+    p.add_argument("--e2e-chunks", type=int, default=0,
                    help="token chunks of the host-buffer entry points in the e2e leg "
                         "when they copy (copies of later chunks overlap the kernels of "
-                        "earlier ones)")
+                        "earlier ones); 0 = chunks of about 48 MiB of rows, at least 2")
+    p.add_argument("--e2e-depth", type=int, default=4,
+                   help="batches in flight in the pipelined e2e leg (one stream and one "
+                        "set of device buffers each)")
     p.add_argument("--e2e-transfer", choices=["auto", "direct", "chunked", "copies"],
                    default="auto",
                    help="e2e leg: direct = the kernels read x from and write y to pinned "
@@ -444,6 +447,15 @@ def pipelined_transfer(requested: str, device_entry_points_only: bool, row_bytes
     return "chunked" if row_bytes >= 2 * (4 << 20) else "direct"
 
 
+def e2e_chunk_count(requested: int, row_bytes: int) -> int:
+    """Token chunks for the copying host-buffer mode: `requested` when set,
+    else chunks of about 48 MiB of x rows, 2 to 8 of them (measured on the
+    pipelined leg: fewer, larger chunks win up to ~60 MB a chunk)."""
+    if requested > 0:
+        return requested
+    return max(2, min(8, row_bytes // (48 << 20)))
+
+
 def path_dtype(wl) -> str:
     """The arithmetic of the path: E4M3 rows (fp32 quantisation) or bf16 bit
     copies on dispatch; the combine folds bf16 rows in fp32 either way."""
@@ -451,11 +463,12 @@ def path_dtype(wl) -> str:
 
 
 def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, idx_h, w_h, recv_x0, Y_d,
-                  chunks, steps, warmup, world, y_want, copies=False):
-    """End to end with two batches in flight, as a serving loop runs: step i
-    goes on stream i % 2 with its own device buffers and host output rows,
-    so one step's combine (y over the host link to the host) overlaps the
-    next step's layout and dispatch (x over the link to the device).  Every
+                  chunks, steps, warmup, world, y_want, copies=False, depth=2):
+    """End to end with `depth` batches in flight, as a serving loop runs:
+    step i goes on stream i % depth with its own device buffers and host
+    output rows, so one step's combine (y over the host link to the host)
+    overlaps later steps' layout and dispatch (x over the link to the
+    device); a step waits only for the step `depth` before it.  Every
     step copies its routes and weights in, reads x from and writes y to
     pinned host memory through the host-buffer entry points (copies=True:
     copies x to the device and y back itself, on the step's stream, around
@@ -474,7 +487,7 @@ def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, idx_h, w_h, r
         pass
 
     slots = []
-    for k in range(2):
+    for k in range(depth):
         sl = Slot()
         sl.stream = stream if k == 0 else torch.cuda.Stream(device)
         sl.sptr = ctypes.c_void_p(sl.stream.cuda_stream)
@@ -523,11 +536,14 @@ def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, idx_h, w_h, r
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         join = torch.cuda.Event()
         a.record(slots[0].stream)
-        slots[1].stream.wait_event(a)
+        for sl in slots[1:]:
+            sl.stream.wait_event(a)
         for i in range(n):
-            step(slots[i % 2])
-        join.record(slots[1].stream)
-        slots[0].stream.wait_event(join)
+            step(slots[i % depth])
+        for sl in slots[1:]:
+            join = torch.cuda.Event()
+            join.record(sl.stream)
+            slots[0].stream.wait_event(join)
         b.record(slots[0].stream)
         return a, b
 
@@ -544,10 +560,10 @@ def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, idx_h, w_h, r
         # same inputs as the sequential leg: the same rows come back
         assert torch.equal(sl.y_h.view(torch.int16), y_want.view(torch.int16))
     return {"value": T * world / (ms / 1e3), "ms_per_step": ms,
-            "pipelining": ("two batches in flight on two streams (step i+1's layout and "
-                           "dispatch overlap step i's combine; each step still moves its own "
-                           "x in and y out); one event pair around all steps, no L2 flush "
-                           "(a step touches far more HBM than L2)")}
+            "pipelining": (f"{depth} batches in flight on {depth} streams (later steps' "
+                           "layout and dispatch overlap a step's combine; each step still "
+                           "moves its own x in and y out); one event pair around all steps, "
+                           "no L2 flush (a step touches far more HBM than L2)")}
 
 
 def workload_config(wl, extra=None):
@@ -818,6 +834,22 @@ def run_ours(args):
         e[ns].record(stream)
     torch.cuda.synchronize()
     barrier(world)
+    # What the layout adds to the chained step: the same steps with the layout
+    # left out (dispatch and combine reuse the layout computed above), events
+    # around each step as in the timed pass.
+    hoisted_ms = None
+    if stages[0][0] == "layout":
+        hev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            l2_flush()
+            hev[i][0].record(stream)
+            for fn in runners[1:]:
+                fn()
+            hev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        hoisted_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in hev)
     # Steady state: the same steps back to back with no flush between them,
     # one event pair around all K, so that each step's write-back of the
     # lines it left dirty in L2 lands inside the timing (of the next step).
@@ -894,6 +926,13 @@ def run_ours(args):
     stream_ms = sum(avg.values())
     breakdown = {"layout_us": (1e3 * statistics.mean(stage_ms["layout"]) if "layout" in stage_ms
                                else None)}
+    if hoisted_ms is not None:
+        breakdown.update({
+            "step_without_layout_us": 1e3 * hoisted_ms,
+            "layout_in_step_us": 1e3 * (ms_local - hoisted_ms),
+            "layout_in_step_note": ("step time minus the same step with the layout left "
+                                    "out: the layout's cost on the chained critical path"),
+        })
     for n in streaming:
         breakdown.update({f"{n}_us": 1e3 * avg[n], f"{n}_median_us": 1e3 * med[n],
                           f"{n}_gbs": gbs[n], f"{n}_pct_of_8tbs": 100 * gbs[n] / NOMINAL_HBM_GBS,
@@ -943,7 +982,7 @@ def run_ours(args):
         # whole.
         transfer = e2e_transfer(args.e2e_transfer, bool(epilogue or fp8_opts))
         host_io = transfer != "copies"
-        chunks = 0 if transfer == "direct" else args.e2e_chunks
+        chunks = 0 if transfer == "direct" else e2e_chunk_count(args.e2e_chunks, T * H * 2)
 
         def e2e_step():
             if not host_io:
@@ -987,11 +1026,11 @@ def run_ours(args):
                       "timing": "one step at a time, L2 flushed before each, events around "
                                 "each step"}
         p_mode = pipelined_transfer(args.e2e_transfer, bool(epilogue or fp8_opts), T * H * 2)
-        p_chunks = args.e2e_chunks if p_mode == "chunked" else 0
+        p_chunks = e2e_chunk_count(args.e2e_chunks, T * H * 2) if p_mode == "chunked" else 0
         pipelined = (pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, idx_h, w_h,
                                    None if wl.use_fp8_dispatch else recv_x, Y_d, p_chunks,
                                    args.steps, args.warmup, world, y_h,
-                                   copies=(p_mode == "copies"))
+                                   copies=(p_mode == "copies"), depth=args.e2e_depth)
                      if p_mode is not None else None)
         e2e = {"unit": "tokens/s",
                "h2d_bytes_per_step": x_h.numel() * 2 + idx_h.numel() * 8 + w_h.numel() * 4,

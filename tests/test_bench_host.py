@@ -71,3 +71,14 @@ def test_cpu_baseline_reports_all_cores_and_one():
 ])
 def test_pipelined_transfer_choice(requested, device_only, row_bytes, want):
     assert bench.pipelined_transfer(requested, device_only, row_bytes) == want
+
+
+@pytest.mark.parametrize("requested,row_bytes,want", [
+    (0, 4096 * 7168 * 2, 2),        # prefill: two chunks of 29 MB
+    (0, 16384 * 7168 * 2, 4),       # 16K tokens: four of 59 MB
+    (0, 8 << 20, 2),                # never fewer than two
+    (0, 1 << 34, 8),                # never more than eight
+    (6, 4096 * 7168 * 2, 6),        # an explicit count stands
+])
+def test_e2e_chunk_count(requested, row_bytes, want):
+    assert bench.e2e_chunk_count(requested, row_bytes) == want
