@@ -456,24 +456,35 @@ def e2e_chunk_count(requested: int, row_bytes: int) -> int:
     return max(2, min(8, row_bytes // (48 << 20)))
 
 
+def route_views(buf, T: int, K: int):
+    """A step's routes (int64 [T, K]) followed by its gate weights (fp32
+    [T, K]) in one uint8 buffer of T*K*12 bytes, so that one copy moves
+    both.  Returns the two views."""
+    import torch
+
+    n = T * K
+    return (buf[: n * 8].view(torch.int64).view(T, K),
+            buf[n * 8: n * 12].view(torch.float32).view(T, K))
+
+
 def path_dtype(wl) -> str:
     """The arithmetic of the path: E4M3 rows (fp32 quantisation) or bf16 bit
     copies on dispatch; the combine folds bf16 rows in fp32 either way."""
     return "fp8_e4m3" if wl.use_fp8_dispatch else "bf16"
 
 
-def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, idx_h, w_h, recv_x0, Y_d,
+def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, route_h, recv_x0, Y_d,
                   chunks, steps, warmup, world, y_want, copies=False, depth=2):
     """End to end with `depth` batches in flight, as a serving loop runs:
     step i goes on stream i % depth with its own device buffers and host
     output rows, so one step's combine (y over the host link to the host)
     overlaps later steps' layout and dispatch (x over the link to the
     device); a step waits only for the step `depth` before it.  Every
-    step copies its routes and weights in, reads x from and writes y to
-    pinned host memory through the host-buffer entry points (copies=True:
-    copies x to the device and y back itself, on the step's stream, around
-    ep_dispatch / ep_combine on device buffers, so that the two copy
-    directions run on their own copy engines).  No L2 flush: a step touches
+    step copies its routes and weights in (one packed copy), reads x from
+    and writes y to pinned host memory through the host-buffer entry points
+    (copies=True: copies x to the device and y back itself, on the step's
+    stream, around ep_dispatch / ep_combine on device buffers, so that the
+    two copy directions run on their own copy engines).  No L2 flush: a step touches
     far more HBM than L2 holds.  Returns the throughput over `steps` steps
     (one event pair around all of them)."""
     import ctypes
@@ -491,8 +502,8 @@ def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, idx_h, w_h, r
         sl = Slot()
         sl.stream = stream if k == 0 else torch.cuda.Stream(device)
         sl.sptr = ctypes.c_void_p(sl.stream.cuda_stream)
-        sl.idx = torch.empty_like(idx_h, device=device)
-        sl.w = torch.empty_like(w_h, device=device)
+        sl.route = torch.empty_like(route_h, device=device)
+        sl.idx, sl.w = route_views(sl.route, T, K)
         sl.L = ep.Layout(cfg, device=device)
         sl.rx = torch.empty((cap, H), dtype=torch.uint8 if wl.use_fp8_dispatch else torch.bfloat16,
                             device=device)
@@ -511,8 +522,7 @@ def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, idx_h, w_h, r
         with torch.cuda.stream(sl.stream):
             if copies:
                 sl.x_d.copy_(x_h, non_blocking=True)
-            sl.idx.copy_(idx_h, non_blocking=True)
-            sl.w.copy_(w_h, non_blocking=True)
+            sl.route.copy_(route_h, non_blocking=True)
         st = ep.ep_get_layout(ccfg, T, p(sl.idx), sl.L.c, None, sl.sptr)
         assert st == 0, ep.ep_status_str(st)
         if copies:
@@ -623,8 +633,10 @@ def run_ours(args):
     ccfg = cfg.c()
 
     x_d = torch.from_numpy(inp["x"].view(np.int16)).to(device).view(torch.bfloat16)
-    idx_d = torch.from_numpy(inp["topk_idx"]).to(device)
-    w_d = torch.from_numpy(inp["topk_weights"]).to(device)
+    route_d = torch.empty(T * K * 12, dtype=torch.uint8, device=device)
+    idx_d, w_d = route_views(route_d, T, K)
+    idx_d.copy_(torch.from_numpy(inp["topk_idx"]))
+    w_d.copy_(torch.from_numpy(inp["topk_weights"]))
     g = torch.Generator(device=device)
     g.manual_seed(1234 + rank)
     Y_d = torch.randn((cap, H), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
@@ -964,8 +976,10 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e and args.pass_ == "forward":
         x_h = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
-        idx_h = torch.from_numpy(inp["topk_idx"]).pin_memory()
-        w_h = torch.from_numpy(inp["topk_weights"]).pin_memory()
+        # routes and gate weights side by side in one pinned buffer: one copy
+        route_h = torch.empty(T * K * 12, dtype=torch.uint8).pin_memory()
+        for v, a in zip(route_views(route_h, T, K), (inp["topk_idx"], inp["topk_weights"])):
+            v.copy_(torch.from_numpy(a))
         y_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
         # Experts: identity for bf16 rows (combine reads the dispatched rows);
         # for E4M3 rows, whose bf16 values no kernel of the path produces, the
@@ -987,8 +1001,7 @@ def run_ours(args):
         def e2e_step():
             if not host_io:
                 x_d.copy_(x_h, non_blocking=True)
-            idx_d.copy_(idx_h, non_blocking=True)
-            w_d.copy_(w_h, non_blocking=True)
+            route_d.copy_(route_h, non_blocking=True)
             layout()
             if host_io:
                 st = ep.ep_dispatch_from_host(ccfg, L.c, x_h.data_ptr(),
@@ -1027,13 +1040,13 @@ def run_ours(args):
                                 "each step"}
         p_mode = pipelined_transfer(args.e2e_transfer, bool(epilogue or fp8_opts), T * H * 2)
         p_chunks = e2e_chunk_count(args.e2e_chunks, T * H * 2) if p_mode == "chunked" else 0
-        pipelined = (pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, idx_h, w_h,
+        pipelined = (pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, route_h,
                                    None if wl.use_fp8_dispatch else recv_x, Y_d, p_chunks,
                                    args.steps, args.warmup, world, y_h,
                                    copies=(p_mode == "copies"), depth=args.e2e_depth)
                      if p_mode is not None else None)
         e2e = {"unit": "tokens/s",
-               "h2d_bytes_per_step": x_h.numel() * 2 + idx_h.numel() * 8 + w_h.numel() * 4,
+               "h2d_bytes_per_step": x_h.numel() * 2 + route_h.numel(),
                "d2h_bytes_per_step": y_h.numel() * 2,
                "experts": ("identity (combine reads the dispatched bf16 rows)"
                            if not wl.use_fp8_dispatch else
