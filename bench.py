@@ -493,6 +493,9 @@ def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, route_h, recv
 
     p = lambda t: None if t is None else t.data_ptr()
     cap = cfg.capacity
+    # no more slots than steps in either run, so that every slot's output is
+    # written (and checked below)
+    depth = max(1, min(depth, max(steps, warmup)))
 
     class Slot:
         pass
