@@ -1048,31 +1048,37 @@ def run_ours(args):
                                    args.steps, args.warmup, world, y_h,
                                    copies=(p_mode == "copies"), depth=args.e2e_depth)
                      if p_mode is not None else None)
+        sequential["transfer"] = (
+            "ep_dispatch_from_host / ep_combine_to_host, direct (the kernels read x and write "
+            "y in pinned host memory)" if transfer == "direct" else
+            f"ep_dispatch_from_host / ep_combine_to_host, {chunks} token chunks (copies "
+            "overlap the kernels)" if host_io else "whole-buffer copies on the stream")
         e2e = {"unit": "tokens/s",
                "h2d_bytes_per_step": x_h.numel() * 2 + route_h.numel(),
                "d2h_bytes_per_step": y_h.numel() * 2,
                "experts": ("identity (combine reads the dispatched bf16 rows)"
                            if not wl.use_fp8_dispatch else
                            "combine reads the device leg's seeded expert-output buffer"),
-               "transfer": ("ep_dispatch_from_host / ep_combine_to_host, direct (the "
-                            "kernels read x and write y in pinned host memory)")
-                           if transfer == "direct" else
-                           (f"ep_dispatch_from_host / ep_combine_to_host, {chunks} token "
-                            "chunks (copies overlap the kernels)") if host_io else
-                           "whole-buffer copies on the stream",
                "sequential": sequential}
         if pipelined is not None:
-            e2e.update(value=pipelined["value"], ms_per_step=pipelined["ms_per_step"],
-                       pipelining=pipelined["pipelining"])
-            e2e["sequential"]["transfer"] = e2e["transfer"]
-            e2e["transfer"] = (
+            pipelined["unit"] = "tokens/s"
+            pipelined["transfer"] = (
                 "ep_dispatch_from_host / ep_combine_to_host, direct (the kernels read x and "
                 "write y in pinned host memory)" if p_mode == "direct" else
                 f"ep_dispatch_from_host / ep_combine_to_host, {p_chunks} token chunks on the "
                 "library's copy streams (one a direction)" if p_mode == "chunked" else
                 "whole-buffer copies on each step's stream around ep_dispatch / ep_combine")
-        else:
-            e2e.update(value=sequential["value"], ms_per_step=e_ms, pipelining=None)
+            e2e["pipelined"] = pipelined
+        # The headline is the faster way to drive the same calls: batches in
+        # flight win wherever a step's device work and transfers outlast the
+        # host's enqueue of a step; with a handful of tokens the host's
+        # per-step calls dominate and one step at a time is faster.
+        best = (pipelined if pipelined is not None and pipelined["value"] >= sequential["value"]
+                else sequential)
+        e2e.update(value=best["value"], ms_per_step=best["ms_per_step"],
+                   mode="pipelined" if best is pipelined else "sequential",
+                   transfer=best["transfer"], pipelining=best.get("pipelining"),
+                   choice="value and ms_per_step are the faster of the legs listed")
 
     # ---- CPU baseline (rank 0, N = 1) ----------------------------------------
     cpu = None
