@@ -90,6 +90,11 @@ def parse_args():
     p.add_argument("--e2e-depth", type=int, default=4,
                    help="batches in flight in the pipelined e2e leg (one stream and one "
                         "set of device buffers each)")
+    p.add_argument("--e2e-graph", choices=["auto", "on", "off"], default="auto",
+                   help="pipelined e2e leg: capture 64 consecutive steps' calls into one "
+                        "CUDA graph and replay it (auto: when the kernels read and write the "
+                        "host rows in place, i.e. small batches, where the host's per-step "
+                        "calls would otherwise set the pace)")
     p.add_argument("--e2e-transfer", choices=["auto", "direct", "chunked", "copies"],
                    default="auto",
                    help="e2e leg: direct = the kernels read x from and write y to pinned "
@@ -447,6 +452,10 @@ def pipelined_transfer(requested: str, device_entry_points_only: bool, row_bytes
     return "chunked" if row_bytes >= 2 * (4 << 20) else "direct"
 
 
+# steps of the pipelined e2e leg captured into one CUDA graph when it replays
+E2E_GRAPH_STEPS = 64
+
+
 def e2e_chunk_count(requested: int, row_bytes: int) -> int:
     """Token chunks for the copying host-buffer mode: `requested` when set,
     else chunks of about 48 MiB of x rows, 2 to 8 of them (measured on the
@@ -474,7 +483,7 @@ def path_dtype(wl) -> str:
 
 
 def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, route_h, recv_x0, Y_d,
-                  chunks, steps, warmup, world, y_want, copies=False, depth=2):
+                  chunks, steps, warmup, world, y_want, copies=False, depth=2, graph_steps=0):
     """End to end with `depth` batches in flight, as a serving loop runs:
     step i goes on stream i % depth with its own device buffers and host
     output rows, so one step's combine (y over the host link to the host)
@@ -484,9 +493,13 @@ def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, route_h, recv
     and writes y to pinned host memory through the host-buffer entry points
     (copies=True: copies x to the device and y back itself, on the step's
     stream, around ep_dispatch / ep_combine on device buffers, so that the
-    two copy directions run on their own copy engines).  No L2 flush: a step touches
-    far more HBM than L2 holds.  Returns the throughput over `steps` steps
-    (one event pair around all of them)."""
+    two copy directions run on their own copy engines).  graph_steps > 0: the
+    same calls for that many consecutive steps (rounded to a multiple of
+    `depth`) are captured once into a CUDA graph, which is replayed, so the
+    host enqueues one launch per graph instead of each step's calls.  No L2
+    flush: a step touches far more HBM than L2 holds, or (small batches)
+    the steps run back to back anyway.  Returns the throughput over at
+    least `steps` steps (one event pair around all of them)."""
     import ctypes
 
     import torch
@@ -503,7 +516,8 @@ def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, route_h, recv
     slots = []
     for k in range(depth):
         sl = Slot()
-        sl.stream = stream if k == 0 else torch.cuda.Stream(device)
+        # (a captured step needs streams of its own: not the legacy default)
+        sl.stream = stream if k == 0 and not graph_steps else torch.cuda.Stream(device)
         sl.sptr = ctypes.c_void_p(sl.stream.cuda_stream)
         sl.route = torch.empty_like(route_h, device=device)
         sl.idx, sl.w = route_views(sl.route, T, K)
@@ -547,7 +561,6 @@ def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, route_h, recv
 
     def run(n):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        join = torch.cuda.Event()
         a.record(slots[0].stream)
         for sl in slots[1:]:
             sl.stream.wait_event(a)
@@ -558,25 +571,58 @@ def pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, route_h, recv
             join.record(sl.stream)
             slots[0].stream.wait_event(join)
         b.record(slots[0].stream)
-        return a, b
+        return a, b, n
+
+    launch = "the calls of each step from the host"
+    if graph_steps > 0:
+        G = depth * max(1, graph_steps // depth)
+        run(depth)   # one-time set-up happens outside the capture
+        torch.cuda.synchronize()
+        cap_s = torch.cuda.Stream(device)
+        cap_s.wait_stream(torch.cuda.current_stream(device))
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap_s):
+            fork = torch.cuda.Event()
+            fork.record(cap_s)
+            for sl in slots:
+                sl.stream.wait_event(fork)
+            for i in range(G):
+                step(slots[i % depth])
+            for sl in slots:
+                join = torch.cuda.Event()
+                join.record(sl.stream)
+                cap_s.wait_event(join)
+        torch.cuda.synchronize()
+        launch = f"one CUDA graph of {G} steps (their calls captured once), replayed"
+
+        def run(n):  # noqa: F811 -- whole replays covering at least n steps
+            reps = max(1, -(-n // G))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cap_s)
+            with torch.cuda.stream(cap_s):
+                for _ in range(reps):
+                    graph.replay()
+            b.record(cap_s)
+            return a, b, reps * G
 
     run(warmup)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    a, b = run(steps)
+    a, b, done = run(steps)
     torch.cuda.synchronize()
     barrier(world)
-    ms = reduce_max(a.elapsed_time(b) / steps, world, device)
+    ms = reduce_max(a.elapsed_time(b) / done, world, device)
     for sl in slots:
         assert ep.ep_check_error(sl.L.c, sl.sptr) == 0
         # same inputs as the sequential leg: the same rows come back
         assert torch.equal(sl.y_h.view(torch.int16), y_want.view(torch.int16))
-    return {"value": T * world / (ms / 1e3), "ms_per_step": ms,
+    return {"value": T * world / (ms / 1e3), "ms_per_step": ms, "steps_timed": done,
+            "launch": launch,
             "pipelining": (f"{depth} batches in flight on {depth} streams (later steps' "
                            "layout and dispatch overlap a step's combine; each step still "
                            "moves its own x in and y out); one event pair around all steps, "
-                           "no L2 flush (a step touches far more HBM than L2)")}
+                           "no L2 flush")}
 
 
 def workload_config(wl, extra=None):
@@ -1043,10 +1089,13 @@ def run_ours(args):
                                 "each step"}
         p_mode = pipelined_transfer(args.e2e_transfer, bool(epilogue or fp8_opts), T * H * 2)
         p_chunks = e2e_chunk_count(args.e2e_chunks, T * H * 2) if p_mode == "chunked" else 0
+        p_graph = (E2E_GRAPH_STEPS if args.e2e_graph == "on" or
+                   (args.e2e_graph == "auto" and p_mode == "direct") else 0)
         pipelined = (pipelined_e2e(ep, ccfg, cfg, T, K, H, wl, device, stream, x_h, route_h,
                                    None if wl.use_fp8_dispatch else recv_x, Y_d, p_chunks,
                                    args.steps, args.warmup, world, y_h,
-                                   copies=(p_mode == "copies"), depth=args.e2e_depth)
+                                   copies=(p_mode == "copies"), depth=args.e2e_depth,
+                                   graph_steps=p_graph)
                      if p_mode is not None else None)
         sequential["transfer"] = (
             "ep_dispatch_from_host / ep_combine_to_host, direct (the kernels read x and write "
@@ -1069,15 +1118,14 @@ def run_ours(args):
                 "library's copy streams (one a direction)" if p_mode == "chunked" else
                 "whole-buffer copies on each step's stream around ep_dispatch / ep_combine")
             e2e["pipelined"] = pipelined
-        # The headline is the faster way to drive the same calls: batches in
-        # flight win wherever a step's device work and transfers outlast the
-        # host's enqueue of a step; with a handful of tokens the host's
-        # per-step calls dominate and one step at a time is faster.
+        # The headline is the faster way to drive the same calls (batches in
+        # flight, graph-replayed for small batches, or one step at a time).
         best = (pipelined if pipelined is not None and pipelined["value"] >= sequential["value"]
                 else sequential)
         e2e.update(value=best["value"], ms_per_step=best["ms_per_step"],
                    mode="pipelined" if best is pipelined else "sequential",
                    transfer=best["transfer"], pipelining=best.get("pipelining"),
+                   launch=best.get("launch", "the calls of each step from the host"),
                    choice="value and ms_per_step are the faster of the legs listed")
 
     # ---- CPU baseline (rank 0, N = 1) ----------------------------------------

@@ -34,6 +34,12 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Work is enqueued asynchronously on it; a call returns before
  *    the GPU has finished unless documented otherwise.
+ *  - Calls that do not synchronise can be recorded into a CUDA graph by
+ *    stream capture: the device entry points, and the host-buffer entry
+ *    points in both modes (in chunked mode the library's copy streams join
+ *    the capture through events; make one chunked call outside any capture
+ *    first, which creates them).  ep_get_layout with h_expert_count,
+ *    ep_check_error and the self-tests synchronise and cannot be captured.
  *  - Argument errors are detected on the host before anything is launched
  *    and returned synchronously (EP_ERR_INVALID_ARG).  Errors in the routing
  *    data (an expert id outside [-1, E), an expert repeated within a token)

@@ -1,7 +1,8 @@
 """GPU checks of the measurement harness itself: the pipelined end-to-end
-leg with fewer steps than batches in flight (every slot that runs is
-checked against a one-step-at-a-time result), and a short default-style
-run of bench.py that must print one JSON line with the contract's keys."""
+leg with fewer steps than batches in flight, issued call by call or
+replayed from a CUDA graph (every slot that runs is checked against a
+one-step-at-a-time result), and a short default-style run of bench.py that
+must print one JSON line with the contract's keys."""
 
 import json
 import os
@@ -57,16 +58,24 @@ def _inputs(ep, wl, device):
 
 @pytest.mark.parametrize("name,chunks", [("tiny", 0), ("decode", 0), ("sweep1k", 2)])
 @pytest.mark.parametrize("steps,warmup", [(1, 1), (2, 1), (3, 6)])
-def test_pipelined_e2e_with_fewer_steps_than_depth(ep, name, chunks, steps, warmup):
+@pytest.mark.parametrize("graph_steps", [0, 64])
+def test_pipelined_e2e_with_fewer_steps_than_depth(ep, name, chunks, steps, warmup, graph_steps):
     wl = workloads.WORKLOADS[name]
     device = torch.device("cuda", 0)
     cfg, x_h, route_h, rx, Y_d, y_want = _inputs(ep, wl, device)
     r = bench.pipelined_e2e(ep, cfg.c(), cfg, wl.num_tokens, wl.num_topk, wl.hidden, wl,
                             device, torch.cuda.current_stream(device), x_h, route_h,
                             None if wl.use_fp8_dispatch else rx, Y_d, chunks, steps, warmup,
-                            1, y_want, depth=4)
+                            1, y_want, depth=4, graph_steps=graph_steps)
     assert r["value"] > 0 and r["ms_per_step"] > 0
-    assert r["pipelining"].startswith(f"{min(4, max(steps, warmup))} batches in flight")
+    depth = min(4, max(steps, warmup))
+    assert r["pipelining"].startswith(f"{depth} batches in flight")
+    if graph_steps:
+        # whole replays of one graph of steps, a multiple of the depth
+        G = depth * (graph_steps // depth)
+        assert r["steps_timed"] == G and f"graph of {G} steps" in r["launch"]
+    else:
+        assert r["steps_timed"] == steps
 
 
 def test_short_bench_run_prints_one_line(ep):
