@@ -82,3 +82,17 @@ def test_pipelined_transfer_choice(requested, device_only, row_bytes, want):
 ])
 def test_e2e_chunk_count(requested, row_bytes, want):
     assert bench.e2e_chunk_count(requested, row_bytes) == want
+
+
+def test_e2e_headline_takes_the_faster_leg():
+    seq = {"value": 2.0, "ms_per_step": 1.0, "transfer": "direct"}
+    pip = {"value": 3.0, "ms_per_step": 0.5, "transfer": "chunked", "pipelining": "4 in flight",
+           "launch": "graph"}
+    h = bench.e2e_headline(seq, pip)
+    assert (h["value"], h["mode"], h["transfer"], h["launch"]) == (3.0, "pipelined", "chunked",
+                                                                   "graph")
+    h = bench.e2e_headline(seq, dict(pip, value=1.0))
+    assert (h["value"], h["mode"], h["transfer"], h["pipelining"]) == (2.0, "sequential",
+                                                                       "direct", None)
+    h = bench.e2e_headline(seq, None)      # options with device entry points only
+    assert h["mode"] == "sequential" and h["ms_per_step"] == 1.0
