@@ -115,6 +115,23 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src,
       : "memory");
 }
 
+// ---- per-thread asynchronous copies ---------------------------------------
+// 16 bytes global -> shared (both 16-byte aligned), cached in L2 only; the
+// issuing thread's copies are complete after cp_async_wait_all, and visible
+// to the CTA after a barrier that follows it.  Completion is tracked by the
+// hardware like a load's, so there is no flag to wait on.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ---- streaming global access ---------------------------------------------
 
 // Row-split kernels: a token's row of 16-byte vectors is shared by

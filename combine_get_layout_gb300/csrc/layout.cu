@@ -653,16 +653,17 @@ __global__ void __launch_bounds__(kAssignThreads)
 // kernel, rows for its own few tokens in (t, k) order, rank rows and
 // padding.  The rows are the same as the two-launch path's.
 struct SmallSmem {
-  int bar, idx, hist, start, total, base, rcnt, rstart, scr, own, rows, bytes;
+  int idx, hist, start, total, base, rcnt, rstart, scr, own, rows, bytes;
 };
 
 // Shared-memory plan of the one-launch layout; with row_bytes > 0 it ends
 // with room for the rows of the CTA's own tokens (fused dispatch, staged).
+// Every region is a multiple of 16 bytes, so the staged rows start on a
+// 16-byte boundary.
 __host__ __device__ inline SmallSmem small_smem(int E, int R, int64_t row_bytes = 0) {
   const int Epad = padded_experts(E), Rpad = padded_ranks(R);
   SmallSmem s;
   int o = 0;
-  s.bar = o;    o += 16;                           // mbarrier of the staged rows
   s.idx = o;    o += kSmallLayoutPairs * 4;        // the routes, checked, packed
   s.hist = o;   o += 3 * Epad * 4;                 // counts: earlier, own, later tokens
   s.start = o;  o += ((E + 1 + 3) & ~3) * 4;
@@ -721,7 +722,6 @@ __global__ void __launch_bounds__(kSmallThreads)
   const int64_t row_bytes = int64_t(d.H) * (kMode != 0 ? 2 : 0);
   const int tt = (T + gridDim.x - 1) / gridDim.x;
   const SmallSmem L = small_smem(E, R, staged ? tt * row_bytes : 0);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
   int32_t* s_idx = reinterpret_cast<int32_t*>(smem + L.idx);      // [T * K]
   int32_t* hist = reinterpret_cast<int32_t*>(smem + L.hist);      // [3][Epad]
   int32_t* s_start = reinterpret_cast<int32_t*>(smem + L.start);
@@ -736,11 +736,7 @@ __global__ void __launch_bounds__(kSmallThreads)
 
   for (int i = tid; i < 3 * Epad; i += blockDim.x) hist[i] = 0;
   for (int i = tid; i < 3 * Rpad; i += blockDim.x) rcnt[i] = 0;
-  if (tid == 0) {
-    s_scr[33] = 0;
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
+  if (tid == 0) s_scr[33] = 0;
   __syncthreads();
   pdl_wait();
 
@@ -750,13 +746,17 @@ __global__ void __launch_bounds__(kSmallThreads)
   const uint32_t eg_magic = div_magic(uint32_t(Eg));
 
   // Fused dispatch with staged rows: the CTA's own x rows (contiguous) are
-  // bulk-copied into shared memory now, so that their DRAM latency passes
-  // while the layout is computed.
+  // copied into shared memory now, 16 bytes a thread at a time
+  // asynchronously, so that their DRAM latency passes while the layout is
+  // computed.  (Per-thread copies rather than one bulk copy: their
+  // completion needs no flag to wait on, so this kernel has no wait that
+  // could give up.)
   const uint32_t stage_bytes = uint32_t((cte - ctb) * row_bytes);
-  if (kMode != 0 && staged && tid == 0 && stage_bytes > 0) {
-    mbar_arrive_expect_tx(bar, stage_bytes);
-    bulk_load(smem + L.rows, reinterpret_cast<const uint8_t*>(d.x) + ctb * row_bytes,
-              stage_bytes, bar);
+  if (kMode != 0 && staged && stage_bytes > 0) {
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(d.x) + ctb * row_bytes;
+    for (uint32_t o = uint32_t(tid) * 16; o < stage_bytes; o += blockDim.x * 16)
+      cp_async16(smem + L.rows + o, src + o);
+    cp_async_commit();
   }
 
   // The whole input, range-checked (an id outside [-1, E) is reported and
@@ -911,21 +911,8 @@ __global__ void __launch_bounds__(kSmallThreads)
   if (kMode == 0) return;
   // Dispatch of this CTA's own tokens to the rows just assigned, from the
   // staged rows in shared memory (or from x when they did not fit).
-  if (staged && stage_bytes > 0) {
-    if (tid == 0) s_scr[32] = mbar_wait(bar, 0, kWaitTimeoutNs);
-    __syncthreads();
-    if (!s_scr[32]) {
-      // the copy did not land in time: report, wait (bounded) once more for
-      // it to finish, and leave without dispatching
-      if (tid == 0) {
-        record_error(err, ERRBIT_TIMEOUT);
-        if (!mbar_wait(bar, 0, kWaitTimeoutNs)) record_error(err, ERRBIT_TIMEOUT_PENDING);
-      }
-      return;
-    }
-  } else {
-    __syncthreads();
-  }
+  if (staged && stage_bytes > 0) cp_async_wait_all();
+  __syncthreads();
   const int nt = cte - ctb;
   const int nvec = d.H >> 3;
   const uint4* srows = reinterpret_cast<const uint4*>(smem + L.rows);  // staged rows

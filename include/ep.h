@@ -221,9 +221,7 @@ EP_API int32_t ep_combine(const ep_config *cfg, const ep_layout *layout,
  * other arrays), then dispatches them as soon as their rows are known, so
  * the dispatch costs no second launch.  Larger inputs run the two paths in
  * turn.  (Column-major scales and pre-quantised input are ep_dispatch_fp8's
- * and are not offered here.)  If the copy of the staged rows were to give
- * up its bounded wait, the error word records EP_ERR_TIMEOUT and those
- * rows are not dispatched.  Returns EP_OK or an error. */
+ * and are not offered here.)  Returns EP_OK or an error. */
 EP_API int32_t ep_layout_and_dispatch(const ep_config *cfg, int32_t num_tokens,
                                       const int64_t *d_topk_idx, ep_layout *layout,
                                       const void *d_x, const float *d_topk_weights,
