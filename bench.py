@@ -1009,6 +1009,7 @@ def run_ours(args):
         })
     for n in streaming:
         breakdown.update({f"{n}_us": 1e3 * avg[n], f"{n}_median_us": 1e3 * med[n],
+                          f"{n}_tokens_per_s": T * world / (avg[n] * 1e-3),
                           f"{n}_gbs": gbs[n], f"{n}_pct_of_8tbs": 100 * gbs[n] / NOMINAL_HBM_GBS,
                           f"{n}_frac_of_measured": gbs[n] / peak})
     breakdown.update({
