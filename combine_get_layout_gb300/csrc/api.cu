@@ -72,7 +72,6 @@ static bool config_ok(const ep_config* c) {
   if (c->zero_padding != 0 && c->zero_padding != 1) return false;
   if (c->use_fp8_dispatch && c->hidden % 128 != 0) return false;
   // bf16 rows: up to the widest row the GPU parity cases cover
-  if (!c->use_fp8_dispatch && c->hidden > 49152) return false;
   // all row indices fit in int32
   const int64_t cap = int64_t(c->max_tokens) * c->num_topk +
                       int64_t(c->num_experts) * (c->expert_alignment - 1);

@@ -88,9 +88,9 @@ enum {
  * count, the expert alignment and the zero-padding switch of dispatch. */
 typedef struct {
   int32_t max_tokens;        /* tokens a layout may hold (capacity planning)   */
-  int32_t hidden;            /* H: bf16 channels per row; H % 8 == 0 and
-                                H <= 49152 for bf16 rows; H % 128 == 0 and
-                                H <= 2^20 when use_fp8_dispatch               */
+  int32_t hidden;            /* H: bf16 channels per row, H <= 2^20; H % 8
+                                == 0 for bf16 rows, H % 128 == 0 when
+                                use_fp8_dispatch                              */
   int32_t num_topk;          /* K in [1, 32], K <= E                           */
   int32_t num_experts;       /* E in [1, 2048]                                  */
   int32_t num_ranks;         /* R logical ranks, E % R == 0; rank r owns the

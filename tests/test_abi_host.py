@@ -65,7 +65,7 @@ def test_capacity_and_workspace(ep):
     dict(num_topk=0), dict(num_topk=33), dict(num_experts=6, num_ranks=4),
     dict(num_topk=9, num_experts=8, num_ranks=2), dict(expert_alignment=0),
     dict(num_ranks=0), dict(max_tokens=-1), dict(max_tokens=2**28, num_topk=16),
-    dict(hidden=49160),                   # bf16 rows wider than 49152 channels
+    dict(hidden=2**20 + 8),               # bf16 rows past 2^20 channels
     dict(hidden=2**20 + 128, use_fp8_dispatch=True),  # E4M3 rows past 2^20
 ])
 def test_invalid_configs_rejected(ep, bad):
@@ -81,7 +81,8 @@ def test_invalid_configs_rejected(ep, bad):
     assert ep.ep_combine(cfg.c(), lay, None, None, None, None) == ep.EP_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("edge", [dict(hidden=49152), dict(hidden=2**20, use_fp8_dispatch=True)])
+@pytest.mark.parametrize("edge", [dict(hidden=49160), dict(hidden=2**20),
+                                  dict(hidden=2**20, use_fp8_dispatch=True)])
 def test_widest_rows_accepted(ep, edge):
     base = dict(max_tokens=64, hidden=256, num_topk=4, num_experts=16,
                 num_ranks=4, expert_alignment=4)

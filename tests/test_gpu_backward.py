@@ -55,6 +55,7 @@ CASES = {
     "k1": workloads.Workload("k1", 257, 256, 16, 1, 16, False, expert_alignment=1),
     "k_eq_e": workloads.Workload("k_eq_e", 64, 256, 32, 32, 4, False, expert_alignment=16),
     "prefill": workloads.WORKLOADS["prefill"],
+    "h_2p20": workloads.Workload("h_2p20", 6, 1 << 20, 4, 2, 2, False, expert_alignment=2),
 }
 
 
@@ -76,7 +77,7 @@ def _tokens(wl):
     return np.unique(np.concatenate([[0, wl.num_tokens - 1], rng.choice(wl.num_tokens, 256)]))
 
 
-@pytest.mark.parametrize("name", ["ragged", "k12", "decode", "k1", "k_eq_e"])
+@pytest.mark.parametrize("name", ["ragged", "k12", "decode", "k1", "k_eq_e", "h_2p20"])
 def test_dispatch_backward_bit_exact(ep, name):
     wl = CASES[name]
     inp, cfg, L, ora = _setup(ep, wl)

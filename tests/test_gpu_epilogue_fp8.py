@@ -41,6 +41,7 @@ CASES = {
                                  expert_alignment=16, mask_frac=0.07),
     "decode": workloads.WORKLOADS["decode"].with_(use_fp8_dispatch=False),
     "small_k1": workloads.Workload("small_k1", 37, 256, 16, 1, 4, False, expert_alignment=8),
+    "h_2p20": workloads.Workload("h_2p20", 6, 1 << 20, 4, 2, 2, False, expert_alignment=2),
 }
 
 
@@ -91,6 +92,7 @@ FP8 = {
                                      expert_alignment=8, mask_frac=0.1),
     "decode": workloads.WORKLOADS["decode"],
     "odd_cap": workloads.Workload("odd_cap", 5, 256, 6, 3, 3, True, expert_alignment=3),
+    "h_2p20_fp8": workloads.Workload("h_2p20_fp8", 6, 1 << 20, 4, 2, 2, True, expert_alignment=2),
 }
 
 

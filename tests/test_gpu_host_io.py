@@ -60,6 +60,9 @@ CASES = {
     "few_tokens": workloads.Workload("few_tokens", 5, 256, 16, 2, 4, False,
                                      expert_alignment=4),
     "prefill": workloads.WORKLOADS["prefill"],
+    # 2 MB rows: 12 MB of x, up to 3 chunks of 2 tokens
+    "h_2p20": workloads.Workload("h_2p20", 6, 1 << 20, 4, 2, 2, False, expert_alignment=2),
+    "h_2p20_fp8": workloads.Workload("h_2p20_fp8", 6, 1 << 20, 4, 2, 2, True, expert_alignment=2),
 }
 
 
@@ -97,7 +100,8 @@ def _rows(L, cfg, zp):
     ("few_tokens", 8, False), ("wide", 3, False), ("wide", 8, True), ("wide", 64, False),
     ("wide_fp8", 5, False), ("wide_fp8", 8, True), ("prefill", 8, False),
     ("ragged", 0, False), ("fp8", 0, True), ("few_tokens", 0, False), ("wide", 0, True),
-    ("wide_fp8", 0, False), ("prefill", 0, False)])
+    ("wide_fp8", 0, False), ("prefill", 0, False),
+    ("h_2p20", 3, True), ("h_2p20", 0, False), ("h_2p20_fp8", 3, False), ("h_2p20_fp8", 0, True)])
 def test_host_buffers_equal_device_buffers(ep, name, chunks, zp):
     wl = CASES[name]
     inp, cfg, L, ref, got, y_ref, h_y = _run(ep, wl, chunks, zp)

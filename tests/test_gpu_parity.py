@@ -639,6 +639,9 @@ EXTREME = {
                                      expert_alignment=4),
     "h_max_fp8": workloads.Workload("h_max_fp8", 24, 49152, 8, 2, 2, True,
                                     expert_alignment=4),
+    # rows of 2^20 channels (the widest accepted; 2 MB bf16 rows)
+    "h_2p20_bf16": workloads.Workload("h_2p20", 6, 1 << 20, 4, 2, 2, False, expert_alignment=2),
+    "h_2p20_fp8": workloads.Workload("h_2p20_fp8", 6, 1 << 20, 4, 2, 2, True, expert_alignment=2),
     "one_expert": workloads.Workload("one_expert", 100, 256, 1, 1, 1, False,
                                      expert_alignment=1),
     "k_eq_e": workloads.Workload("k_eq_e", 64, 256, 32, 32, 4, False, expert_alignment=16),

@@ -52,6 +52,7 @@ CASES = {
                                    mask_frac=0.05),
     "rank_per_expert": workloads.Workload("rank_per_expert", 200, 256, 16, 4, 16, False,
                                           expert_alignment=4),
+    "h_2p20": workloads.Workload("h_2p20", 6, 1 << 20, 4, 2, 2, False, expert_alignment=2),
 }
 
 
@@ -98,7 +99,7 @@ def test_rank_rows_through_noalloc_entry_point(ep):
     assert np.array_equal(L.rank_src.cpu().numpy()[: rl["rows"]], rl["rank_src"][: rl["rows"]])
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "r64", "r64_small", "skew", "one_rank",
+@pytest.mark.parametrize("name", ["tiny", "ragged", "r64", "r64_small", "skew", "one_rank", "h_2p20",
                                   "rank_per_expert"])
 def test_dispatch_ranks_and_expand(ep, name):
     wl = CASES[name]
@@ -126,7 +127,7 @@ def test_dispatch_ranks_and_expand(ep, name):
     assert torch.equal(recv[:used].view(torch.int16), direct[:used].view(torch.int16))
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "r64", "r64_small", "skew", "prefill",
+@pytest.mark.parametrize("name", ["tiny", "ragged", "r64", "r64_small", "skew", "prefill", "h_2p20",
                                   "one_rank", "rank_per_expert"])
 @pytest.mark.parametrize("weighted", [True, False])
 def test_reduce_and_combine_ranks(ep, name, weighted):
